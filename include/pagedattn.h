@@ -1,0 +1,214 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so, attention over a paged KV cache on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The four operations are the per-layer GPU hot path of a Nano-vLLM-style
+ * serving engine, as described on these pages:
+ *   [LIFE] "一个 prompt 的一生：nano-vllm 从起服务到吐出 token" (violet-quartz.github.io)
+ *   [UML]  the Nano-vLLM walk-through at uml.org.cn
+ *   [SRC2] "《Nano-vLLM源码逐行解析》第2篇 sequence.py、scheduler.py" (yeyulingfeng.com)
+ *
+ * Data layout (all row-major, contiguous):
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim] bf16: one
+ *                     layer's view of the KV pool ([LIFE] §2.2.3; [UML] §3.2).
+ *                     A slot s is row s of the pool viewed as
+ *                     [num_blocks*block_size, num_kv_heads, head_dim].
+ *   block_tables      [batch, max_blocks_per_seq] int32: logical block i of a
+ *                     sequence -> physical block id ([UML] §1 Step2, §3.2).
+ *                     Entries past a sequence's last block are never read.
+ *   q                 [tokens, num_q_heads, head_dim] bf16; k, v [tokens,
+ *                     num_kv_heads, head_dim] bf16 ([UML] §3.2 formats).
+ *   Grouped-query attention: q head h reads kv head h / (num_q_heads/num_kv_heads).
+ *
+ * Ownership: every pointer argument is caller-owned memory; the library keeps
+ * no pointer past the call, allocates nothing and never synchronises.  Device
+ * pointers must be device memory of the current CUDA device.  All work is
+ * enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ * stream) and runs asynchronously.
+ *
+ * Errors, two kinds:
+ *   - the return value: PKV_OK (0) or a negative PKV_ERR_* code for a problem
+ *     the host can see (null pointer, bad size, unsupported head_dim,
+ *     misaligned pointer, workspace too small, launch failure).  Nothing is
+ *     enqueued when a call returns an error.
+ *   - `status`: an optional device uint32 into which kernels OR the
+ *     PKV_STATUS_* bits of data-dependent problems (a slot or block id outside
+ *     the pool, a bad context length, ...).  The offending item is skipped
+ *     (its outputs are zeros where the entry point says so); nothing traps.
+ *     The caller clears the word; NULL disables reporting.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define PKV_OK                        0
+#define PKV_ERR_NULL_POINTER         -1
+#define PKV_ERR_BAD_DIMENSION        -2
+#define PKV_ERR_UNSUPPORTED_HEAD_DIM -3
+#define PKV_ERR_MISALIGNED           -4
+#define PKV_ERR_WORKSPACE_TOO_SMALL  -5
+#define PKV_ERR_CUDA                 -6
+#define PKV_ERR_UNSUPPORTED          -7
+
+/* ---- device status bits ------------------------------------------------ */
+#define PKV_STATUS_SLOT_OUT_OF_RANGE  (1u << 0) /* kv_store: slot >= num_blocks*block_size   */
+#define PKV_STATUS_BAD_BLOCK_ID       (1u << 1) /* a block table entry outside [0,num_blocks) */
+#define PKV_STATUS_BAD_CONTEXT_LEN    (1u << 2) /* context len < 0, > table capacity or > max */
+#define PKV_STATUS_BAD_SEQLENS        (1u << 3) /* cu_seqlens not monotone, Lk < Lq, ...       */
+#define PKV_STATUS_BAD_TEMPERATURE    (1u << 4) /* sample: temperature not positive & finite  */
+#define PKV_STATUS_NO_FINITE_KEY      (1u << 5) /* sample: every key of a row is NaN           */
+#define PKV_STATUS_WORKSPACE_OVERFLOW (1u << 6) /* more work items than the workspace holds   */
+#define PKV_STATUS_WAIT_TIMEOUT       (1u << 7) /* a bounded in-kernel wait gave up           */
+
+/* One layer's KV cache geometry: k_cache/v_cache are [num_blocks, block_size,
+ * num_kv_heads, head_dim] bf16. */
+typedef struct pkv_cache_desc {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} pkv_cache_desc;
+
+/* Library version, major*10000 + minor*100 + patch. */
+PKV_API int pkv_version(void);
+
+/* Text for a PKV_ERR_* return code (static storage). */
+PKV_API const char* pkv_error_string(int code);
+
+/* Text naming the lowest PKV_STATUS_* bit set in `bits` ("ok" for 0). */
+PKV_API const char* pkv_status_string(uint32_t bits);
+
+/*
+ * kv_store -- the per-layer KV cache write ("store_kvcache").
+ * [UML] §2.4 (KV written into the cache before attention), §1 Step2 (slot =
+ * blockID*blockSize + loc); [LIFE] §3.3.2 / §4 (slot_mapping holds one
+ * physical slot per flattened token, so the writer needs no paging logic).
+ *
+ *   k, v           device, [num_tokens, num_kv_heads, head_dim] bf16, 16-byte aligned
+ *   k_cache/v_cache device, the pool, written in place, 16-byte aligned
+ *   slot_mapping   device, [num_tokens] int32; slot < 0 skips the token (padding
+ *                  rows of a fixed-shape batch); slot >= num_blocks*block_size
+ *                  sets PKV_STATUS_SLOT_OUT_OF_RANGE and skips it
+ * Row i of k and of v is copied bit for bit into slot slot_mapping[i].  Two
+ * tokens with the same slot in one call: the surviving row is one of them.
+ * Needs num_kv_heads*head_dim*2 to be a multiple of 16.  num_tokens == 0 is a
+ * no-op.
+ */
+PKV_API int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
+                 const int32_t* slot_mapping, int32_t num_tokens,
+                 pkv_cache_desc cache, uint32_t* status, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode needs for these sizes (a pure
+ * host function; the same arguments give the same answer).
+ */
+PKV_API size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                        int32_t max_context_len, pkv_cache_desc cache);
+
+/*
+ * paged_decode -- decode attention, one query token per sequence, K/V read
+ * through the block table ([UML] §2.4: the decode attention op; §3.2: Q as
+ * (batch, 1, heads, head_dim), cache_seqlens, block_tables).
+ *
+ *   q             device, [batch, num_q_heads, head_dim] bf16
+ *   k_cache/v_cache device, the pool (read only)
+ *   block_tables  device, [batch, max_blocks_per_seq] int32
+ *   context_lens  device, [batch] int32: keys of sequence b are its logical
+ *                 positions 0..context_lens[b]-1 (the new token's K/V must
+ *                 already be stored).  0 gives a zero output row.  A value < 0,
+ *                 > max_blocks_per_seq*block_size or > max_context_len sets
+ *                 PKV_STATUS_BAD_CONTEXT_LEN and gives zeros.
+ *   max_context_len host upper bound of context_lens, sizes the split-KV grid
+ *   scale         softmax scale (e.g. 1/sqrt(head_dim))
+ *   out           device, [batch, num_q_heads, head_dim] bf16
+ *   workspace     device, >= pkv_paged_decode_workspace_bytes(...) bytes,
+ *                 16-byte aligned; holds the split-KV partial results
+ * out[b,h] = sum_j softmax_j(scale * q[b,h].K_j) V_j, fp32 accumulation.
+ * head_dim 64 or 128; num_q_heads a multiple of num_kv_heads.
+ */
+PKV_API int pkv_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                     int32_t max_context_len, float scale, void* out,
+                     void* workspace, size_t workspace_bytes,
+                     pkv_cache_desc cache, uint32_t* status, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_prefill_varlen needs (pure host function).
+ */
+PKV_API size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,
+                                         int32_t num_q_heads, pkv_cache_desc cache);
+
+/*
+ * paged_prefill_varlen -- causal prefill over a flattened batch of
+ * variable-length sequences whose first tokens may already be in the cache
+ * (prefix caching, chunked prefill).  [UML] §2.4 and §3.2 (the varlen prefill
+ * attention op: cu_seqlens_q/k, max_seqlen_q/k, block_tables when a prefix is
+ * cached); [LIFE] §3.1 / [SRC2] Sequence walkthrough (a round computes
+ * num_scheduled_tokens tokens starting at num_cached_tokens).
+ *
+ *   q             device, [total_q, num_q_heads, head_dim] bf16
+ *   k, v          device, [total_q, num_kv_heads, head_dim] bf16: this call's
+ *                 own keys/values, one row per query token
+ *   k_cache/v_cache device, the pool (read only)
+ *   cu_seqlens_q/k device, [batch+1] int32 prefix sums.  Sequence b has
+ *                 Lq = cu_q[b+1]-cu_q[b] queries and Lk = cu_k[b+1]-cu_k[b] keys.
+ *                 Keys j < Lk-Lq (the cached prefix) are read from the cache
+ *                 through block_tables[b]; keys j >= Lk-Lq are rows
+ *                 cu_q[b]+j-(Lk-Lq) of k/v.  Query i sits at position Lk-Lq+i
+ *                 and attends keys j <= Lk-Lq+i (bottom-right causal).
+ *   max_seqlen_q/k host upper bounds of Lq/Lk
+ *   block_tables  device [batch, max_blocks_per_seq] int32, or NULL when no
+ *                 sequence has a cached prefix (then Lk must equal Lq)
+ *   out           device, [total_q, num_q_heads, head_dim] bf16
+ *   workspace     device, >= pkv_paged_prefill_workspace_bytes(...) bytes,
+ *                 16-byte aligned; holds the tile schedule
+ * A sequence with inconsistent lengths sets PKV_STATUS_BAD_SEQLENS and is
+ * skipped (its output rows are not written).  head_dim 64 or 128.
+ */
+PKV_API int pkv_paged_prefill_varlen(const void* q, const void* k, const void* v,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             int32_t batch, int32_t total_q, int32_t max_seqlen_q,
+                             int32_t max_seqlen_k, int32_t num_q_heads,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             float scale, void* out, void* workspace, size_t workspace_bytes,
+                             pkv_cache_desc cache, uint32_t* status, void* stream);
+
+/*
+ * sample -- temperature, softmax and Gumbel-max sampling of one token per row
+ * ([UML] §2.4: "温度、softmax和gumbel max"; [LIFE] §4: the sampler runs on each
+ * sequence's last-position logits).  With supplied Exp(1) noise E the draw is
+ * argmax_i softmax(logits/T)_i / E_i, computed as the equal
+ * argmax_i (logits_i/T - ln max(E_i, 1e-10)); ties go to the lowest index.
+ *
+ *   logits        device, [batch, vocab] fp32
+ *   temperatures  device, [batch] fp32; a value that is not positive and finite
+ *                 sets PKV_STATUS_BAD_TEMPERATURE and the row returns 0
+ *   exp_noise     device, [batch, vocab] fp32 Exp(1) draws
+ *   out_token_ids device, [batch] int32
+ * NaN keys never win; a row of NaN keys returns 0 and sets
+ * PKV_STATUS_NO_FINITE_KEY.
+ */
+PKV_API int pkv_sample(const float* logits, const float* temperatures, const float* exp_noise,
+               int32_t batch, int32_t vocab, int32_t* out_token_ids,
+               uint32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,237 @@
+"""ctypes binding of libpagedattn.so: argument marshalling only.
+
+Every function checks the tensors' device, dtype and contiguity, passes raw
+device pointers, sizes and the current CUDA stream to the C ABI declared in
+include/pagedattn.h, and raises on a non-zero return code.  All arithmetic
+runs in the library's CUDA kernels; there is no other implementation here, and
+a missing library is an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+_LIB = None
+
+PKV_STATUS_BITS = {
+    1 << 0: "SLOT_OUT_OF_RANGE",
+    1 << 1: "BAD_BLOCK_ID",
+    1 << 2: "BAD_CONTEXT_LEN",
+    1 << 3: "BAD_SEQLENS",
+    1 << 4: "BAD_TEMPERATURE",
+    1 << 5: "NO_FINITE_KEY",
+    1 << 6: "WORKSPACE_OVERFLOW",
+    1 << 7: "WAIT_TIMEOUT",
+}
+STATUS = {v: k for k, v in PKV_STATUS_BITS.items()}
+
+C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_store",
+               "pkv_paged_decode_workspace_bytes", "pkv_paged_decode",
+               "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample"]
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads libpagedattn.so (built by __graft_entry__.build() or
+    paged_kv_attention_scatter_gb300._build.build()).  Raises if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run paged_kv_attention_scatter_gb300._build."
+                           "build() (or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    lib.pkv_version.restype = ctypes.c_int
+    lib.pkv_version.argtypes = []
+    lib.pkv_error_string.restype = ctypes.c_char_p
+    lib.pkv_error_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_status_string.argtypes = [ctypes.c_uint32]
+    lib.pkv_kv_store.restype = ctypes.c_int
+    lib.pkv_kv_store.argtypes = [P, P, P, P, P, I32, CacheDesc, P, P]
+    lib.pkv_paged_decode_workspace_bytes.restype = SZ
+    lib.pkv_paged_decode_workspace_bytes.argtypes = [I32, I32, I32, CacheDesc]
+    lib.pkv_paged_decode.restype = ctypes.c_int
+    lib.pkv_paged_decode.argtypes = [P, P, P, P, I32, P, I32, I32, I32, F32, P, P, SZ,
+                                     CacheDesc, P, P]
+    lib.pkv_paged_prefill_workspace_bytes.restype = SZ
+    lib.pkv_paged_prefill_workspace_bytes.argtypes = [I32, I32, I32, CacheDesc]
+    lib.pkv_paged_prefill_varlen.restype = ctypes.c_int
+    lib.pkv_paged_prefill_varlen.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P,
+                                             I32, F32, P, P, SZ, CacheDesc, P, P]
+    lib.pkv_sample.restype = ctypes.c_int
+    lib.pkv_sample.argtypes = [P, P, P, I32, I32, P, P, P]
+    _LIB = lib
+    return lib
+
+
+# ----------------------------------------------------------------------------
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        msg = load().pkv_error_string(rc).decode()
+        raise RuntimeError(f"{what}: {msg} (code {rc})")
+
+
+def _dev(t: torch.Tensor, name: str, dtype, device=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t.data_ptr()
+
+
+def _ptr_or_null(t, name, dtype, device):
+    return None if t is None else _dev(t, name, dtype, device)
+
+
+def _stream(device, stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    nb, bs, hkv, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d)
+
+
+def new_status(device) -> torch.Tensor:
+    """A zeroed device status word for the `status=` argument."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def status_names(word: int) -> list[str]:
+    return [n for b, n in PKV_STATUS_BITS.items() if word & b]
+
+
+# ----------------------------------------------------------------------------
+def kv_store(k, v, k_cache, v_cache, slot_mapping, status=None, stream=None) -> None:
+    """Writes row i of k / v into slot slot_mapping[i] of k_cache / v_cache
+    (in place).  k, v: [N, Hkv, D] bf16; caches [NB, bs, Hkv, D] bf16;
+    slot_mapping [N] int32 (negative = skip)."""
+    lib = load()
+    dev = k_cache.device
+    n = slot_mapping.numel()
+    if k.shape != (n,) + tuple(k_cache.shape[2:]) or v.shape != k.shape:
+        raise ValueError("k/v must be [num_tokens, num_kv_heads, head_dim] matching the cache")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    rc = lib.pkv_kv_store(_dev(k, "k", torch.bfloat16, dev), _dev(v, "v", torch.bfloat16, dev),
+                          _dev(k_cache, "k_cache", torch.bfloat16, dev),
+                          _dev(v_cache, "v_cache", torch.bfloat16, dev),
+                          _dev(slot_mapping, "slot_mapping", torch.int32, dev), n,
+                          cache_desc(k_cache), _ptr_or_null(status, "status", torch.int32, dev),
+                          _stream(dev, stream))
+    _check(rc, "pkv_kv_store")
+
+
+def paged_decode_workspace_bytes(batch, num_q_heads, max_context_len, k_cache) -> int:
+    return int(load().pkv_paged_decode_workspace_bytes(batch, num_q_heads, max_context_len,
+                                                       cache_desc(k_cache)))
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                 out=None, workspace=None, status=None, stream=None) -> torch.Tensor:
+    """Decode attention: q [B, Hq, D] bf16 -> out [B, Hq, D] bf16.
+    block_tables [B, MB] int32, context_lens [B] int32, max_context_len a host
+    upper bound of context_lens."""
+    lib = load()
+    dev = k_cache.device
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_decode_workspace_bytes(B, Hq, max_context_len, k_cache)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.pkv_paged_decode(_dev(q, "q", torch.bfloat16, dev),
+                              _dev(k_cache, "k_cache", torch.bfloat16, dev),
+                              _dev(v_cache, "v_cache", torch.bfloat16, dev),
+                              _dev(block_tables, "block_tables", torch.int32, dev),
+                              block_tables.shape[1],
+                              _dev(context_lens, "context_lens", torch.int32, dev), B, Hq,
+                              int(max_context_len), float(scale),
+                              _dev(out, "out", torch.bfloat16, dev),
+                              _dev(workspace, "workspace", torch.uint8, dev), workspace.numel(),
+                              cache_desc(k_cache),
+                              _ptr_or_null(status, "status", torch.int32, dev),
+                              _stream(dev, stream))
+    _check(rc, "pkv_paged_decode")
+    return out
+
+
+def paged_prefill_workspace_bytes(batch, total_q, num_q_heads, k_cache_shape) -> int:
+    nb, bs, hkv, d = k_cache_shape
+    return int(load().pkv_paged_prefill_workspace_bytes(batch, total_q, num_q_heads,
+                                                        CacheDesc(nb, bs, hkv, d)))
+
+
+def paged_prefill_varlen(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                         max_seqlen_k, block_tables, scale, out=None, workspace=None,
+                         status=None, stream=None) -> torch.Tensor:
+    """Causal varlen prefill: q [Tq, Hq, D], k/v [Tq, Hkv, D] bf16 -> out
+    [Tq, Hq, D] bf16.  k_cache/v_cache and block_tables may be None when no
+    sequence has a cached prefix."""
+    lib = load()
+    dev = q.device
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    shape = tuple(k_cache.shape) if k_cache is not None else (1, 1, Hkv, D)
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_prefill_workspace_bytes(B, T, Hq, shape)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    desc = CacheDesc(*shape)
+    rc = lib.pkv_paged_prefill_varlen(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k, "k", torch.bfloat16, dev),
+        _dev(v, "v", torch.bfloat16, dev),
+        _ptr_or_null(k_cache, "k_cache", torch.bfloat16, dev),
+        _ptr_or_null(v_cache, "v_cache", torch.bfloat16, dev),
+        _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev),
+        _dev(cu_seqlens_k, "cu_seqlens_k", torch.int32, dev), B, T, int(max_seqlen_q),
+        int(max_seqlen_k), Hq, _ptr_or_null(block_tables, "block_tables", torch.int32, dev),
+        block_tables.shape[1] if block_tables is not None else 0, float(scale),
+        _dev(out, "out", torch.bfloat16, dev), _dev(workspace, "workspace", torch.uint8, dev),
+        workspace.numel(), desc, _ptr_or_null(status, "status", torch.int32, dev),
+        _stream(dev, stream))
+    _check(rc, "pkv_paged_prefill_varlen")
+    return out
+
+
+def sample(logits, temperatures, exp_noise, out=None, status=None, stream=None) -> torch.Tensor:
+    """Gumbel-max sampling: logits, exp_noise [B, V] fp32, temperatures [B]
+    fp32 -> token ids [B] int32."""
+    lib = load()
+    dev = logits.device
+    B, V = logits.shape
+    if exp_noise.shape != logits.shape or temperatures.shape != (B,):
+        raise ValueError("shape mismatch between logits, temperatures and exp_noise")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib.pkv_sample(_dev(logits, "logits", torch.float32, dev),
+                        _dev(temperatures, "temperatures", torch.float32, dev),
+                        _dev(exp_noise, "exp_noise", torch.float32, dev), B, V,
+                        _dev(out, "out", torch.int32, dev),
+                        _ptr_or_null(status, "status", torch.int32, dev), _stream(dev, stream))
+    _check(rc, "pkv_sample")
+    return out

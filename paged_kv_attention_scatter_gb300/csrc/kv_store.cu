@@ -1,0 +1,71 @@
+// kv_store: scatter each new token's K and V rows into the paged cache.
+//
+// The per-layer cache write of a Nano-vLLM-style engine (uml.org.cn
+// walk-through §2.4 and "KV cache的写入函数"; "一个 prompt 的一生" §3.3.2, §4):
+// slot_mapping[i] is the physical slot of flattened token i, a slot being
+// row block_id*block_size + offset of the pool viewed as
+// [num_blocks*block_size, Hkv, D].  The writer needs no other paging logic, so
+// the kernel is a row scatter: token i's K row (Hkv*D bf16, contiguous) goes
+// to pool row slot_mapping[i], and the same for V.
+//
+// Design: one 16-byte vector per thread per tensor; a warp covers 512
+// contiguous bytes of a row, so both the read of k/v and the write of the
+// cache row are fully coalesced.  Loads are issued for K and V before either
+// store to keep two requests in flight per thread.  HBM traffic = 2 reads +
+// 2 writes of Hkv*D*2 bytes per token: the roofline is pure bandwidth.
+#include "common.cuh"
+
+namespace {
+
+__global__ void __launch_bounds__(256) kv_store_kernel(
+        const uint4* __restrict__ k, const uint4* __restrict__ v,
+        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+        const int32_t* __restrict__ slot_mapping, int32_t num_tokens,
+        int32_t row_vecs, int64_t num_slots, uint32_t* status) {
+    const int64_t total = (int64_t)num_tokens * row_vecs;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += stride) {
+        const int32_t t = (int32_t)(idx / row_vecs);
+        const int32_t c = (int32_t)(idx - (int64_t)t * row_vecs);
+        const int32_t s = __ldg(slot_mapping + t);
+        if (s < 0) continue;                                  // padding row
+        if ((int64_t)s >= num_slots) {
+            if (c == 0) pkv::report(status, PKV_STATUS_SLOT_OUT_OF_RANGE);
+            continue;
+        }
+        const uint4 kv = pkv::ld_stream16(k + idx);
+        const uint4 vv = pkv::ld_stream16(v + idx);
+        const int64_t dst = (int64_t)s * row_vecs + c;
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+}  // namespace
+
+extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
+                            const int32_t* slot_mapping, int32_t num_tokens,
+                            pkv_cache_desc cache, uint32_t* status, void* stream) {
+    if (num_tokens < 0) return PKV_ERR_BAD_DIMENSION;
+    if (cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0 ||
+        cache.head_dim <= 0)
+        return PKV_ERR_BAD_DIMENSION;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_NULL_POINTER;
+    const int64_t row_bytes = (int64_t)cache.num_kv_heads * cache.head_dim * 2;
+    if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED_HEAD_DIM;
+    if (((uintptr_t)k | (uintptr_t)v | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return PKV_ERR_MISALIGNED;
+    if (((uintptr_t)slot_mapping) & 3) return PKV_ERR_MISALIGNED;
+    const int32_t row_vecs = (int32_t)(row_bytes / 16);
+    const int64_t total = (int64_t)num_tokens * row_vecs;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = (int64_t)pkv_num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    kv_store_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        (const uint4*)k, (const uint4*)v, (uint4*)k_cache, (uint4*)v_cache, slot_mapping,
+        num_tokens, row_vecs, (int64_t)cache.num_blocks * cache.block_size, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

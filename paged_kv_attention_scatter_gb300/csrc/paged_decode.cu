@@ -1,0 +1,487 @@
+// paged_decode: split-KV (flash-decoding) attention for one query token per
+// sequence, K/V read through a per-sequence block table.
+//
+// What it computes (uml.org.cn walk-through §2.4: the decode attention op over
+// the paged cache with cache_seqlens and block_tables; §3.2 tensor formats):
+// out[b,h] = sum_{j < ctx_b} softmax_j(scale * q[b,h] . K_j) V_j, where key j
+// of sequence b is row j % bs of physical block block_tables[b][j / bs] and
+// q head h reads kv head h / G (G = Hq / Hkv, grouped-query attention).
+//
+// Design for GB300 (HBM-bound: every cache byte is read once):
+//  * Work unit = (sequence, kv head, group of <= 8 q heads, chunk of keys).  A
+//    one-CTA plan kernel writes each sequence's chunk count as a prefix sum in
+//    the workspace; the persistent main grid (SMs x resident CTAs) walks the
+//    units round-robin, so empty units cost nothing and nothing depends on a
+//    host-side length (the launch is graph-capturable).
+//  * Inside a unit each of the 4 warps takes 16-key steps.  K and V rows are
+//    loaded straight from HBM into mma.sync fragments with 16-byte loads (a
+//    warp reads 8 rows x 64 B of K and 4 rows x 128 B of V per instruction):
+//      S   = Q K^T   : M = the q heads of the group (rows 0..7 of m16), N = 8
+//                      keys, K = head_dim.  The head_dim order of the K
+//                      fragment is a fixed permutation applied to Q as well,
+//                      so each thread loads contiguous 16-byte chunks.
+//      O^T = V^T P^T : M = head_dim (16 per tile), N = the q heads, K = 16
+//                      keys.  The S accumulator of two key tiles is exactly
+//                      the P^T operand, so P never leaves registers; V's
+//                      transpose is done by byte permutes of row pairs.
+//    The dot products run on the tensor pipe, which keeps the kernel
+//    memory-bound even for a group of 8 (8 flop per cache byte).
+//  * Online softmax in base 2 with warp-shuffle row maxima; the 4 warps of a
+//    CTA merge through shared memory; units of a sequence with more than one
+//    chunk write (m, l, unnormalised o) to the workspace and a combine kernel
+//    merges them.  A sequence with a single chunk is written directly.
+//  * Keys past ctx_b are never loaded (their registers are zero and their
+//    scores -inf), so NaN in unused cache slots cannot reach the output.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStep = 16;            // keys per warp step
+constexpr int kMaxGroup = 8;         // q heads per unit (mma rows 0..7)
+
+struct DecodeArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* kc;
+    const __nv_bfloat16* vc;
+    const int32_t* bt;
+    const int32_t* ctx;
+    __nv_bfloat16* out;
+    int32_t* chunk_prefix;           // [B+1] exclusive prefix of chunk counts
+    float2* part_ml;                 // [cap * Hq]: (max, sum) in base 2
+    float* part_o;                   // [cap * Hq * D]
+    int32_t B, Hq, Hkv, G, n_hg, MB, NB, bs, max_ctx, chunk_keys, cap;
+    float scale_log2;
+    uint32_t* status;
+};
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// pack (lo = element e of a, hi = element e of b), e in 0..7 of a 16-byte chunk
+__device__ __forceinline__ uint32_t pair(const uint4& a, const uint4& b, int e) {
+    return __byte_perm(word(a, e >> 1), word(b, e >> 1), (e & 1) ? 0x7632 : 0x5410);
+}
+
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int64_t cap_keys = (int64_t)a.MB * a.bs;
+    for (int32_t base = 0; base < a.B; base += blockDim.x) {
+        const int32_t b = base + threadIdx.x;
+        int32_t n = 0;
+        if (b < a.B) {
+            const int32_t c = a.ctx[b];
+            if (c < 0 || c > cap_keys || c > a.max_ctx) {
+                pkv::report(a.status, PKV_STATUS_BAD_CONTEXT_LEN);
+            } else {
+                n = (c + a.chunk_keys - 1) / a.chunk_keys;
+            }
+        }
+        // block-wide inclusive scan of n
+        int32_t x = n;
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_sums[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int32_t s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            warp_sums[lane] = s;
+        }
+        __syncthreads();
+        const int32_t incl = x + (w > 0 ? warp_sums[w - 1] : 0) + carry;
+        if (b < a.B) a.chunk_prefix[b + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) a.chunk_prefix[0] = 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
+    constexpr int NQ = D / 32;       // 16-byte chunks per thread of a Q / K row
+    constexpr int KK = D / 16;       // k-steps of S = Q K^T
+    constexpr int MT = D / 16;       // m-tiles of O^T
+    __shared__ float sm_m[kWarps][kMaxGroup];
+    __shared__ float sm_l[kWarps][kMaxGroup];
+    __shared__ float sm_o[kWarps][kMaxGroup][D];
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int units_per_sc = a.Hkv * a.n_hg;
+    const int32_t total_sc = a.chunk_prefix[a.B];
+    const int64_t units = (int64_t)total_sc * units_per_sc;
+    const bool fast_bs = (a.bs % kStep) == 0;
+    const int64_t row_elems = (int64_t)a.Hkv * D;
+
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int32_t sc = (int32_t)(u / units_per_sc);
+        const int32_t rem = (int32_t)(u - (int64_t)sc * units_per_sc);
+        const int32_t kvh = rem / a.n_hg, hg = rem - kvh * a.n_hg;
+        // sequence owning chunk slot sc: the last b with prefix[b] <= sc
+        int32_t lo = 0, hi = a.B;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (a.chunk_prefix[mid] <= sc) lo = mid; else hi = mid - 1;
+        }
+        const int32_t b = lo;
+        const int32_t chunk = sc - a.chunk_prefix[b];
+        const int32_t nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
+        const int32_t ctx = a.ctx[b];
+        const int32_t key0 = chunk * a.chunk_keys;
+        const int32_t key_end = min(ctx, key0 + a.chunk_keys);
+        const int32_t h0 = kvh * a.G + hg * kMaxGroup;
+        const int32_t nh = min(kMaxGroup, a.G - hg * kMaxGroup);
+        const int32_t* bt_row = a.bt + (int64_t)b * a.MB;
+        const __nv_bfloat16* kbase = a.kc + (int64_t)kvh * D;
+        const __nv_bfloat16* vbase = a.vc + (int64_t)kvh * D;
+
+        // Q fragment: row g = head h0+g, chunks i*4+t (the fixed head_dim order)
+        uint4 qv[NQ];
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            qv[i] = make_uint4(0, 0, 0, 0);
+            if (g < nh)
+                qv[i] = *reinterpret_cast<const uint4*>(
+                    a.q + ((int64_t)b * a.Hq + h0 + g) * D + (i * 4 + t) * 8);
+        }
+        float o[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool bad_block = false;
+
+        for (int32_t step = key0 + warp * kStep; step < key_end; step += kWarps * kStep) {
+            // ---- row addresses (nullptr: not loaded, treated as masked) ----
+            const __nv_bfloat16* krow[2];
+            const __nv_bfloat16* vrow[4];
+            const int vkey[4] = {step + 2 * t, step + 2 * t + 1, step + 2 * t + 8,
+                                 step + 2 * t + 9};
+            if (fast_bs) {
+                const int32_t blk = bt_row[step / a.bs];
+                const int32_t off = step % a.bs;
+                const bool ok = (unsigned)blk < (unsigned)a.NB;
+                bad_block |= !ok;
+                const int64_t r0 = ((int64_t)blk * a.bs + off) * row_elems;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int key = step + r * 8 + g;
+                    krow[r] = (ok && key < key_end) ? kbase + r0 + (int64_t)(r * 8 + g) * row_elems
+                                                    : nullptr;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    vrow[r] = (ok && vkey[r] < key_end)
+                                  ? vbase + r0 + (int64_t)(vkey[r] - step) * row_elems
+                                  : nullptr;
+            } else {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int key = step + r * 8 + g;
+                    krow[r] = nullptr;
+                    if (key < key_end) {
+                        const int32_t blk = bt_row[key / a.bs];
+                        if ((unsigned)blk < (unsigned)a.NB)
+                            krow[r] = kbase + ((int64_t)blk * a.bs + key % a.bs) * row_elems;
+                        else
+                            bad_block = true;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    vrow[r] = nullptr;
+                    if (vkey[r] < key_end) {
+                        const int32_t blk = bt_row[vkey[r] / a.bs];
+                        if ((unsigned)blk < (unsigned)a.NB)
+                            vrow[r] = vbase + ((int64_t)blk * a.bs + vkey[r] % a.bs) * row_elems;
+                        else
+                            bad_block = true;
+                    }
+                }
+            }
+            // ---- loads: K rows step+g, step+8+g; V rows 2t, 2t+1, 2t+8, 2t+9 ----
+            uint4 kr[2][NQ];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int i = 0; i < NQ; ++i)
+                    kr[r][i] = krow[r] ? pkv::ld_stream16(krow[r] + (i * 4 + t) * 8)
+                                       : make_uint4(0, 0, 0, 0);
+            constexpr int VC = (D == 128) ? 2 : 1;          // chunks per V row
+            uint4 vr[4][VC];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < VC; ++c)
+                    vr[r][c] = vrow[r] ? pkv::ld_stream16(vrow[r] + (g + 8 * c) * 8)
+                                       : make_uint4(0, 0, 0, 0);
+            // ---- S = Q K^T for two 8-key tiles ----
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KK; ++kk) {
+                    const int i = kk >> 1, w0 = 2 * (kk & 1);
+                    pkv::mma_bf16_16816(s[nt], word(qv[i], w0), 0u, word(qv[i], w0 + 1), 0u,
+                                        word(kr[nt][i], w0), word(kr[nt][i], w0 + 1));
+                }
+            }
+            // ---- online softmax (base 2) for head g over keys 2t,2t+1,8+2t,9+2t ----
+            float x[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int nt = j >> 1, e = j & 1;
+                x[j] = vrow[j] ? s[nt][e] * a.scale_log2 : -INFINITY;
+            }
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = (m_run == -INFINITY) ? 0.f : pkv::fast_exp2(m_run - m_use);
+            float p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) p[j] = pkv::fast_exp2(x[j] - m_use);
+            l_run = l_run * alpha + (p[0] + p[1]) + (p[2] + p[3]);
+            m_run = m_new;
+            const float alpha_a = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
+            const float alpha_b = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
+            const uint32_t b0 = pkv::pack_bf16(p[0], p[1]);
+            const uint32_t b1 = pkv::pack_bf16(p[2], p[3]);
+            // ---- O^T = V^T P^T ----
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][0] *= alpha_a; o[mt][1] *= alpha_b;
+                o[mt][2] *= alpha_a; o[mt][3] *= alpha_b;
+                uint32_t a0, a1, a2, a3;
+                if (D == 128) {
+                    a0 = pair(vr[0][0], vr[1][0], mt);
+                    a1 = pair(vr[0][VC - 1], vr[1][VC - 1], mt);
+                    a2 = pair(vr[2][0], vr[3][0], mt);
+                    a3 = pair(vr[2][VC - 1], vr[3][VC - 1], mt);
+                } else {
+                    a0 = pair(vr[0][0], vr[1][0], mt);
+                    a1 = pair(vr[0][0], vr[1][0], 4 + mt);
+                    a2 = pair(vr[2][0], vr[3][0], mt);
+                    a3 = pair(vr[2][0], vr[3][0], 4 + mt);
+                }
+                pkv::mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+            }
+        }
+        if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
+
+        // ---- per-warp results to shared memory ----
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+        if (t == 0) {
+            sm_m[warp][g] = m_run;
+            sm_l[warp][g] = l_run;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            // O^T rows: d of fragment row g and row g+8 of m-tile mt
+            const int d_lo = (D == 128) ? 8 * g + mt : 8 * g + mt;
+            const int d_hi = (D == 128) ? 64 + 8 * g + mt : 8 * g + 4 + mt;
+            sm_o[warp][2 * t][d_lo] = o[mt][0];
+            sm_o[warp][2 * t + 1][d_lo] = o[mt][1];
+            sm_o[warp][2 * t][d_hi] = o[mt][2];
+            sm_o[warp][2 * t + 1][d_hi] = o[mt][3];
+        }
+        __syncthreads();
+        // ---- merge the 4 warps: thread -> (head, d) ----
+        for (int idx = threadIdx.x; idx < nh * D; idx += kThreads) {
+            const int h = idx / D, d = idx - h * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
+            float L = 0.f, O = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float mw = sm_m[w][h];
+                    if (mw == -INFINITY) continue;
+                    const float f = pkv::fast_exp2(mw - M);
+                    L += sm_l[w][h] * f;
+                    O += sm_o[w][h][d] * f;
+                }
+            }
+            const int64_t qh = (int64_t)b * a.Hq + h0 + h;
+            if (nch == 1) {
+                a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            } else {
+                const int64_t slot = (int64_t)sc * a.Hq + h0 + h;
+                a.part_o[slot * D + d] = O;
+                if (d == 0) a.part_ml[slot] = make_float2(M, L);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
+    const int32_t h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
+    if (n == 1) return;                                  // written by the split kernel
+    const int64_t qh = (int64_t)b * a.Hq + h;
+    if (n == 0) {                                        // empty or rejected sequence
+        a.out[qh * D + d] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    float M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmaxf(M, a.part_ml[(int64_t)(p0 + c) * a.Hq + h].x);
+    float L = 0.f, O = 0.f;
+    for (int c = 0; c < n; ++c) {
+        const int64_t slot = (int64_t)(p0 + c) * a.Hq + h;
+        const float2 ml = a.part_ml[slot];
+        if (ml.x == -INFINITY) continue;
+        const float f = pkv::fast_exp2(ml.x - M);
+        L += ml.y * f;
+        O += a.part_o[slot * D + d] * f;
+    }
+    a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+}
+
+// Keys per work unit: a multiple of 64 (4 warps x 16), chosen from the sizes
+// alone so the workspace query and the call agree.  Larger chunks cut the
+// partial-result traffic; smaller ones give the persistent grid more units.
+int32_t choose_chunk_keys(int32_t batch, int32_t units_per_seq_chunk, int32_t max_ctx) {
+    const int64_t want_units = 8LL * 152 * 3;            // ~8 units per resident CTA
+    int32_t chunk = 1024;
+    while (chunk > 64) {
+        const int64_t per_seq = ((int64_t)max_ctx / 2 + chunk - 1) / chunk;
+        if ((int64_t)batch * units_per_seq_chunk * per_seq >= want_units) break;
+        chunk >>= 1;
+    }
+    return chunk;
+}
+
+struct DecodeLayout {
+    int32_t chunk_keys, cap;
+    size_t off_prefix, off_ml, off_o, total;
+};
+
+DecodeLayout decode_layout(int32_t batch, int32_t num_q_heads, int32_t max_ctx,
+                           const pkv_cache_desc& c) {
+    DecodeLayout L{};
+    const int32_t G = num_q_heads / (c.num_kv_heads > 0 ? c.num_kv_heads : 1);
+    const int32_t n_hg = (G + kMaxGroup - 1) / kMaxGroup;
+    L.chunk_keys = choose_chunk_keys(batch, c.num_kv_heads * n_hg, max_ctx);
+    const int64_t per_seq = ((int64_t)max_ctx + L.chunk_keys - 1) / L.chunk_keys;
+    L.cap = (int32_t)((int64_t)batch * per_seq);
+    auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    L.off_prefix = 0;
+    L.off_ml = align(L.off_prefix + sizeof(int32_t) * ((size_t)batch + 1));
+    L.off_o = align(L.off_ml + sizeof(float2) * (size_t)L.cap * num_q_heads);
+    L.total = align(L.off_o + sizeof(float) * (size_t)L.cap * num_q_heads * c.head_dim);
+    return L;
+}
+
+template <int D>
+int max_resident(const void* fn) {
+    static int cached[2] = {-1, -1};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& slot = cached[D == 128 ? 1 : 0];
+    if (slot < 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        slot = n;
+    }
+    return slot;
+}
+
+template <int D>
+int launch_decode(DecodeArgs& a, cudaStream_t s) {
+    decode_plan_kernel<<<1, 1024, 0, s>>>(a);
+    const int per_sm = max_resident<D>((const void*)decode_split_kernel<D>);
+    const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;
+    int64_t grid = (int64_t)pkv_num_sms() * per_sm;
+    if (grid > upper) grid = upper;
+    if (grid < 1) grid = 1;
+    decode_split_kernel<D><<<(unsigned)grid, kThreads, 0, s>>>(a);
+    for (int32_t b0 = 0; b0 < a.B; b0 += 65535) {
+        DecodeArgs sub = a;
+        const int32_t rows = a.B - b0 < 65535 ? a.B - b0 : 65535;
+        sub.chunk_prefix = a.chunk_prefix + b0;
+        sub.out = a.out + (int64_t)b0 * a.Hq * D;
+        decode_combine_kernel<D><<<dim3((unsigned)a.Hq, (unsigned)rows), D, 0, s>>>(sub);
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                                   int32_t max_context_len,
+                                                   pkv_cache_desc cache) {
+    if (batch < 0 || num_q_heads <= 0 || max_context_len < 0 || cache.num_kv_heads <= 0 ||
+        cache.head_dim <= 0)
+        return 0;
+    return decode_layout(batch, num_q_heads, max_context_len, cache).total;
+}
+
+extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t batch,
+                                int32_t num_q_heads, int32_t max_context_len, float scale,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                pkv_cache_desc cache, uint32_t* status, void* stream) {
+    if (batch < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 ||
+        cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0)
+        return PKV_ERR_BAD_DIMENSION;
+    if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_BAD_DIMENSION;
+    if (cache.head_dim != 64 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED_HEAD_DIM;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return PKV_ERR_NULL_POINTER;
+    if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out |
+         (uintptr_t)workspace) & 15)
+        return PKV_ERR_MISALIGNED;
+    if (((uintptr_t)block_tables | (uintptr_t)context_lens) & 3) return PKV_ERR_MISALIGNED;
+    const DecodeLayout L = decode_layout(batch, num_q_heads, max_context_len, cache);
+    if (workspace_bytes < L.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    char* ws = (char*)workspace;
+    DecodeArgs a;
+    a.q = (const __nv_bfloat16*)q;
+    a.kc = (const __nv_bfloat16*)k_cache;
+    a.vc = (const __nv_bfloat16*)v_cache;
+    a.bt = block_tables;
+    a.ctx = context_lens;
+    a.out = (__nv_bfloat16*)out;
+    a.chunk_prefix = (int32_t*)(ws + L.off_prefix);
+    a.part_ml = (float2*)(ws + L.off_ml);
+    a.part_o = (float*)(ws + L.off_o);
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cache.num_kv_heads;
+    a.G = num_q_heads / cache.num_kv_heads;
+    a.n_hg = (a.G + kMaxGroup - 1) / kMaxGroup;
+    a.MB = max_blocks_per_seq;
+    a.NB = cache.num_blocks;
+    a.bs = cache.block_size;
+    a.max_ctx = max_context_len;
+    a.chunk_keys = L.chunk_keys;
+    a.cap = L.cap;
+    a.scale_log2 = scale * pkv::kLog2e;
+    a.status = status;
+    cudaStream_t s = (cudaStream_t)stream;
+    return cache.head_dim == 128 ? launch_decode<128>(a, s) : launch_decode<64>(a, s);
+}

@@ -1,0 +1,47 @@
+// Shared pieces of the varlen prefill kernels: arguments, the tile schedule.
+#pragma once
+
+#include "common.cuh"
+
+namespace pkv {
+
+struct PrefillArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* kc;
+    const __nv_bfloat16* vc;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    const int32_t* bt;               // may be null
+    __nv_bfloat16* out;
+    int32_t* sched;                  // [0]=tile count, [1]=dispatch counter, [2..3] spare
+    int2* tiles;                     // (sequence, q tile) pairs, heaviest first
+    int32_t B, total_q, max_sq, max_sk, Hq, Hkv, G, MB, NB, bs, max_tiles;
+    int32_t tile_m, tile_n;          // tile shape the schedule is built for
+    float scale_log2;
+    uint32_t* status;
+};
+
+// Lengths of sequence b; returns false (and reports) when they are inconsistent.
+__device__ __forceinline__ bool seq_lengths(const PrefillArgs& a, int32_t b, int32_t& q0,
+                                            int32_t& lq, int32_t& lk, bool report_bad) {
+    q0 = a.cu_q[b];
+    lq = a.cu_q[b + 1] - q0;
+    lk = a.cu_k[b + 1] - a.cu_k[b];
+    const int32_t c = lk - lq;
+    bool ok = lq >= 0 && c >= 0 && q0 >= 0 && q0 + lq <= a.total_q;
+    if (c > 0) ok = ok && a.bt != nullptr && (int64_t)(c + a.bs - 1) / a.bs <= a.MB;
+    if (!ok && report_bad) report(a.status, PKV_STATUS_BAD_SEQLENS);
+    return ok;
+}
+
+}  // namespace pkv
+
+struct PrefillLayout {
+    size_t off_sched, off_tiles, total;
+    int32_t max_tiles;
+};
+
+PrefillLayout pkv_prefill_layout(int32_t batch, int32_t total_q);
+int pkv_launch_prefill_plan(pkv::PrefillArgs& a, cudaStream_t s);

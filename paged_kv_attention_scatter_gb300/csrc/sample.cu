@@ -1,0 +1,163 @@
+// sample: temperature, softmax and Gumbel-max, one token per row.
+//
+// The uml.org.cn walk-through (§2.4 Model Runner) states the sampler as
+// temperature, then softmax, then a Gumbel-max draw; "一个 prompt 的一生" §4
+// applies it to each sequence's last-position logits.  With Exp(1) noise E
+// supplied, the draw argmax_i softmax(x)_i / E_i (x = logits / T) equals
+// argmax_i (x_i - ln E_i): softmax is a monotone map of x within a row and its
+// normaliser is common to the row.  So one streaming pass per row suffices:
+// no max, no exp, no sum -- each element costs one multiply, one log and one
+// compare, and the row is read exactly once (8 bytes per vocabulary entry).
+//
+// Design: a thread-block cluster of up to 8 CTAs owns one row; each CTA scans a
+// contiguous segment with 16-byte streaming loads, reduces its best
+// (key, index) by warp shuffles and shared memory, and rank 0 of the cluster
+// gathers the CTAs' results over distributed shared memory.  Ties keep the
+// lowest index at every level, so the result does not depend on the split.
+// No workspace and no second launch: the cluster barrier is a hardware
+// barrier of co-scheduled CTAs, not a spin on memory.
+#include <cooperative_groups.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kNoiseFloor = 1e-10f;
+
+struct Cand {
+    float key;
+    int idx;
+};
+
+__device__ __forceinline__ void take_if_better(Cand& a, float key, int idx) {
+    if (key > a.key || (key == a.key && idx < a.idx)) {
+        a.key = key;
+        a.idx = idx;
+    }
+}
+
+__device__ __forceinline__ float gumbel_key(float logit, float inv_t, float e) {
+    return logit * inv_t - __logf(fmaxf(e, kNoiseFloor));
+}
+
+__global__ void __launch_bounds__(kThreads) sample_kernel(
+        const float* __restrict__ logits, const float* __restrict__ temperatures,
+        const float* __restrict__ noise, int32_t row0, int32_t vocab, bool vec_ok,
+        int32_t* __restrict__ out, uint32_t* status) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int csize = (int)cluster.num_blocks();
+    const int64_t row = (int64_t)row0 + blockIdx.y;
+
+    __shared__ float warp_key[kThreads / 32];
+    __shared__ int warp_idx[kThreads / 32];
+    __shared__ Cand cta_best;
+
+    const float temp = temperatures[row];
+    const bool t_ok = isfinite(temp) && temp > 0.f;
+    Cand best{-CUDART_INF_F, INT_MAX};
+    if (t_ok) {
+        const float inv_t = 1.0f / temp;
+        const float* lrow = logits + row * vocab;
+        const float* nrow = noise + row * vocab;
+        // contiguous segment of this CTA, a multiple of 4 entries long
+        int seg = (vocab + csize - 1) / csize;
+        seg = (seg + 3) & ~3;
+        const int lo = min(vocab, rank * seg);
+        const int hi = min(vocab, lo + seg);
+        if (vec_ok) {
+            // rows start 16-byte aligned: lo is a multiple of 4
+            const int nvec = (hi - lo) >> 2;
+            for (int v = threadIdx.x; v < nvec; v += kThreads) {
+                const int i = lo + 4 * v;
+                const float4 l4 = pkv::ld_stream16f(lrow + i);
+                const float4 e4 = pkv::ld_stream16f(nrow + i);
+                take_if_better(best, gumbel_key(l4.x, inv_t, e4.x), i);
+                take_if_better(best, gumbel_key(l4.y, inv_t, e4.y), i + 1);
+                take_if_better(best, gumbel_key(l4.z, inv_t, e4.z), i + 2);
+                take_if_better(best, gumbel_key(l4.w, inv_t, e4.w), i + 3);
+            }
+            for (int i = lo + 4 * nvec + threadIdx.x; i < hi; i += kThreads)
+                take_if_better(best, gumbel_key(lrow[i], inv_t, nrow[i]), i);
+        } else {
+            for (int i = lo + threadIdx.x; i < hi; i += kThreads)
+                take_if_better(best, gumbel_key(lrow[i], inv_t, nrow[i]), i);
+        }
+    }
+    // warp, then CTA
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float k2 = __shfl_xor_sync(0xffffffffu, best.key, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, best.idx, off);
+        take_if_better(best, k2, i2);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        warp_key[warp] = best.key;
+        warp_idx[warp] = best.idx;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Cand c{warp_key[0], warp_idx[0]};
+        for (int w = 1; w < kThreads / 32; ++w) take_if_better(c, warp_key[w], warp_idx[w]);
+        cta_best = c;
+    }
+    cluster.sync();                       // every CTA's cta_best is written
+    if (rank == 0 && threadIdx.x == 0) {
+        Cand c = cta_best;
+        for (int r = 1; r < csize; ++r) {
+            const Cand* other = cluster.map_shared_rank(&cta_best, r);
+            take_if_better(c, other->key, other->idx);
+        }
+        int32_t tok = 0;
+        if (!t_ok) {
+            pkv::report(status, PKV_STATUS_BAD_TEMPERATURE);
+        } else if (c.idx == INT_MAX) {
+            pkv::report(status, PKV_STATUS_NO_FINITE_KEY);
+        } else {
+            tok = c.idx;
+        }
+        out[row] = tok;
+    }
+    cluster.sync();                       // keep shared memory alive for rank 0
+}
+
+}  // namespace
+
+extern "C" int pkv_sample(const float* logits, const float* temperatures,
+                          const float* exp_noise, int32_t batch, int32_t vocab,
+                          int32_t* out_token_ids, uint32_t* status, void* stream) {
+    if (batch < 0 || vocab <= 0) return PKV_ERR_BAD_DIMENSION;
+    if (batch == 0) return PKV_OK;
+    if (!logits || !temperatures || !exp_noise || !out_token_ids) return PKV_ERR_NULL_POINTER;
+    if (((uintptr_t)logits | (uintptr_t)temperatures | (uintptr_t)exp_noise |
+         (uintptr_t)out_token_ids) & 3)
+        return PKV_ERR_MISALIGNED;
+    const bool vec_ok = (vocab % 4 == 0) && ((((uintptr_t)logits) | ((uintptr_t)exp_noise)) & 15) == 0;
+    int csize = (vocab + 16383) / 16384;           // about 16K entries per CTA
+    if (csize > 8) csize = 8;
+    if (csize < 1) csize = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    for (int32_t r0 = 0; r0 < batch; r0 += 65535) {
+        const int32_t rows = batch - r0 < 65535 ? batch - r0 : 65535;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)csize, (unsigned)rows, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = (cudaStream_t)stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel, logits, temperatures, exp_noise,
+                                           r0, vocab, vec_ok, out_token_ids, status);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

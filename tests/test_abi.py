@@ -1,0 +1,74 @@
+"""The C ABI library builds for sm_103a, loads, and exports every symbol the
+header declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_scatter_gb300 import _binding, _build
+    _build.build()
+    return _binding.load()
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("pkv_kv_store", "pkv_paged_decode", "pkv_paged_prefill_varlen", "pkv_sample"):
+        assert op in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    from paged_kv_attention_scatter_gb300 import _binding
+    assert sorted(_binding.C_FUNCTIONS) == declared_functions()
+
+
+def test_version_and_strings(lib):
+    assert lib.pkv_version() >= 100
+    assert lib.pkv_error_string(0) == b"ok"
+    assert b"null" in lib.pkv_error_string(-1)
+    assert lib.pkv_status_string(0) == b"ok"
+    assert b"slot" in lib.pkv_status_string(1)
+
+
+def test_workspace_queries_are_pure(lib):
+    from paged_kv_attention_scatter_gb300._binding import CacheDesc
+    c = CacheDesc(610, 256, 8, 128)
+    a = lib.pkv_paged_decode_workspace_bytes(64, 16, 4096, c)
+    assert a == lib.pkv_paged_decode_workspace_bytes(64, 16, 4096, c) and a > 0
+    assert lib.pkv_paged_decode_workspace_bytes(64, 16, 8192, c) >= a
+    p = lib.pkv_paged_prefill_workspace_bytes(16, 16384, 32, c)
+    assert p >= 8 * (16384 // 64 + 16)
+
+
+def test_host_checks_return_codes_without_a_gpu(lib):
+    from paged_kv_attention_scatter_gb300._binding import CacheDesc
+    c = CacheDesc(8, 4, 1, 64)
+    # empty calls are no-ops that launch nothing
+    assert lib.pkv_kv_store(None, None, None, None, None, 0, c, None, None) == 0
+    assert lib.pkv_sample(None, None, None, 0, 10, None, None, None) == 0
+    # argument errors are reported before any CUDA call
+    assert lib.pkv_kv_store(None, None, None, None, None, 3, c, None, None) == -1
+    assert lib.pkv_kv_store(None, None, None, None, None, -1, c, None, None) == -2
+    bad = CacheDesc(8, 4, 1, 96)
+    assert lib.pkv_paged_decode(None, None, None, None, 1, None, 1, 1, 8, 1.0, None, None, 0,
+                                bad, None, None) == -3
+    assert lib.pkv_paged_decode(None, None, None, None, 1, None, 1, 3, 8, 1.0, None, None, 0,
+                                CacheDesc(8, 4, 2, 64), None, None) == -2
+    assert lib.pkv_paged_prefill_varlen(None, None, None, None, None, None, None, 1, 4, 4, 4,
+                                        2, None, 0, 1.0, None, None, 0, c, None, None) == -1
+    # a misaligned pointer is rejected on the host; it is never dereferenced
+    p = ctypes.c_void_p(16 * 1024 + 2)
+    assert lib.pkv_sample(p, p, p, 1, 10, p, None, None) == -4

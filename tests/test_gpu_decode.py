@@ -1,0 +1,148 @@
+"""paged_decode on the GPU against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as U
+from oracle import attention as oatt
+from oracle import kv_store as okv
+from paged_kv_attention_scatter_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(pkv, w, dev, seqs=None, status_expect=0, max_ctx=None):
+    st = pkv.new_status(dev)
+    out = pkv.paged_decode(w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev),
+                           w.block_tables.to(dev), w.context_lens.to(dev), w.scale,
+                           max_ctx if max_ctx is not None else w.max_context_len, status=st)
+    assert U.status_word(st) == status_expect
+    kc = w.k_cache.cpu() if w.k_cache.is_cuda else w.k_cache
+    vc = w.v_cache.cpu() if w.v_cache.is_cuda else w.v_cache
+    ref = oatt.paged_decode(U.f64(w.q), kc, vc, w.block_tables.numpy(),
+                            w.context_lens.numpy(), w.scale, seqs=seqs)
+    got = U.f64(out)
+    idx = list(range(w.q.shape[0])) if seqs is None else list(seqs)
+    return U.assert_close(got[idx], ref[idx], w.spec.name)
+
+
+def test_tiny_decode_steps(cuda):
+    pkv = U.lib()
+    w = W.tiny_workload()
+    kc, vc = U.bits(w.k_cache0), U.bits(w.v_cache0)
+    p = w.prefill
+    kc, vc, _ = okv.kv_store(U.bits(p.k), U.bits(p.v), kc, vc, p.slot_mapping.numpy())
+    for st in w.decode_steps:
+        kc, vc, _ = okv.kv_store(U.bits(st.k_new), U.bits(st.v_new), kc, vc,
+                                 st.slot_mapping.numpy())
+        kt = torch.from_numpy(kc).view(torch.bfloat16)
+        vt = torch.from_numpy(vc).view(torch.bfloat16)
+        out = pkv.paged_decode(st.q.to(cuda), kt.to(cuda), vt.to(cuda),
+                               st.block_tables.to(cuda), st.context_lens.to(cuda), w.scale,
+                               int(st.context_lens.max()))
+        ref = oatt.paged_decode(U.f64(st.q), kt, vt, st.block_tables.numpy(),
+                                st.context_lens.numpy(), w.scale)
+        U.assert_close(U.f64(out), ref, "tiny decode")
+
+
+def test_decode_0p6b_full_batch(cuda):
+    pkv = U.lib()
+    w = W.decode_workload(W.DECODE_0P6B)
+    err, rel = _decode(pkv, w, cuda)
+    print(f"decode-0.6b: max abs {err:.3g}, rel L2 {rel:.3g}")
+
+
+def test_decode_32b_skewed_sampled(cuda):
+    pkv = U.lib()
+    w = W.decode_workload(W.DECODE_32B, device=cuda)
+    ctx = w.context_lens.numpy()
+    order = np.argsort(ctx)
+    seqs = sorted(set(order[:3].tolist() + order[-3:].tolist() + [7, 100, 201]))
+    err, rel = _decode(pkv, w, cuda, seqs=seqs)
+    print(f"decode-32b sampled {seqs}: max abs {err:.3g}, rel L2 {rel:.3g}")
+
+
+def test_step_8b_store_then_decode_sampled(cuda):
+    pkv = U.lib()
+    w = W.decode_workload(W.STEP_8B, device=cuda)
+    st = pkv.new_status(cuda)
+    kc, vc = w.k_cache, w.v_cache
+    seqs = [0, 1, 77, 255, 300, 511]
+    # oracle-side cache: the sequences' blocks before the step, then the store
+    kc_cpu, vc_cpu = kc.cpu(), vc.cpu()
+    pkv.kv_store(w.k_new, w.v_new, kc, vc, w.slot_mapping.to(cuda), status=st)
+    out = pkv.paged_decode(w.q, kc, vc, w.block_tables.to(cuda), w.context_lens.to(cuda),
+                           w.scale, w.max_context_len, status=st)
+    assert U.status_word(st) == 0
+    ok, ov, _ = okv.kv_store(U.bits(w.k_new), U.bits(w.v_new), U.bits(kc_cpu), U.bits(vc_cpu),
+                             w.slot_mapping.numpy())
+    ref = oatt.paged_decode(U.f64(w.q), torch.from_numpy(ok).view(torch.bfloat16),
+                            torch.from_numpy(ov).view(torch.bfloat16), w.block_tables.numpy(),
+                            w.context_lens.numpy(), w.scale, seqs=seqs)
+    U.assert_close(U.f64(out)[seqs], ref[seqs], "step-8b decode")
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs", [(4, 4, 128, 16), (16, 1, 128, 256), (8, 2, 64, 4),
+                                         (6, 2, 64, 32), (12, 4, 128, 64)])
+def test_shapes_and_block_sizes(cuda, hq, hkv, d, bs):
+    pkv = U.lib()
+    spec = W.DecodeSpec(f"shape {hq}/{hkv}x{d} bs{bs}", seed=hq * 31 + bs, batch=7,
+                        num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                        ctx_lo=1, ctx_hi=700)
+    w = W.decode_workload(spec)
+    _decode(pkv, w, cuda)
+
+
+def test_zero_and_one_key_contexts(cuda):
+    pkv = U.lib()
+    spec = W.DecodeSpec("edge", seed=9, batch=5, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                        block_size=16, ctx_lo=1, ctx_hi=40)
+    w = W.decode_workload(spec)
+    w.context_lens[0] = 0
+    w.context_lens[1] = 1
+    _decode(pkv, w, cuda)
+
+
+def test_context_over_stated_maximum_is_reported(cuda):
+    pkv = U.lib()
+    spec = W.DecodeSpec("over", seed=10, batch=4, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                        block_size=16, ctx_lo=20, ctx_hi=60)
+    w = W.decode_workload(spec)
+    st = pkv.new_status(cuda)
+    lim = int(w.context_lens.min())
+    out = pkv.paged_decode(w.q.to(cuda), w.k_cache.to(cuda), w.v_cache.to(cuda),
+                           w.block_tables.to(cuda), w.context_lens.to(cuda), w.scale, lim,
+                           status=st)
+    assert U.status_word(st) == pkv.STATUS["BAD_CONTEXT_LEN"]
+    over = (w.context_lens > lim).nonzero().flatten().tolist()
+    assert over and float(out[over].abs().max()) == 0.0
+
+
+def test_bad_block_id_is_reported_not_read(cuda):
+    pkv = U.lib()
+    spec = W.DecodeSpec("badblk", seed=12, batch=3, num_q_heads=4, num_kv_heads=1,
+                        head_dim=128, block_size=16, ctx_lo=40, ctx_hi=60)
+    w = W.decode_workload(spec)
+    w.block_tables[1, 1] = 10_000_000
+    st = pkv.new_status(cuda)
+    out = pkv.paged_decode(w.q.to(cuda), w.k_cache.to(cuda), w.v_cache.to(cuda),
+                           w.block_tables.to(cuda), w.context_lens.to(cuda), w.scale,
+                           w.max_context_len, status=st)
+    assert U.status_word(st) == pkv.STATUS["BAD_BLOCK_ID"]
+    assert torch.isfinite(out.float()).all()
+    ref = oatt.paged_decode(U.f64(w.q), w.k_cache, w.v_cache, w.block_tables.numpy(),
+                            w.context_lens.numpy(), w.scale, seqs=[0, 2])
+    U.assert_close(U.f64(out)[[0, 2]], ref[[0, 2]], "unaffected sequences")
+
+
+def test_workspace_too_small_is_rejected(cuda):
+    pkv = U.lib()
+    w = W.decode_workload(W.DecodeSpec("ws", seed=1, batch=2, num_q_heads=2, num_kv_heads=1,
+                                       head_dim=64, block_size=16, ctx_lo=5, ctx_hi=9))
+    ws = torch.empty(16, dtype=torch.uint8, device=cuda)
+    with pytest.raises(RuntimeError, match="workspace"):
+        pkv.paged_decode(w.q.to(cuda), w.k_cache.to(cuda), w.v_cache.to(cuda),
+                         w.block_tables.to(cuda), w.context_lens.to(cuda), w.scale,
+                         w.max_context_len, workspace=ws)

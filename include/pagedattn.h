@@ -147,6 +147,36 @@ PKV_API int pkv_paged_decode(const void* q, const void* k_cache, const void* v_c
                      pkv_cache_desc cache, uint32_t* status, void* stream);
 
 /*
+ * paged_decode without a caller-provided workspace.  (Not an operation of the
+ * pages: it exists for callers that cannot allocate device memory where they
+ * call -- e.g. a plugin inside a host engine that owns and budgets all device
+ * memory up front, or a latency-critical loop that must not pay for
+ * cudaMalloc's implicit device-wide synchronisation.)
+ *
+ * Same arguments and results as pkv_paged_decode, minus workspace and
+ * workspace_bytes.  The split-KV scratch is a fixed array of
+ * PKV_STATIC_DECODE_WORKSPACE_BYTES compiled into the library; every GPU that
+ * loads the library holds it until the process exits.  The call allocates
+ * nothing (no cudaMalloc, no allocating library routine).
+ *   - When pkv_paged_decode_workspace_bytes(batch, num_q_heads,
+ *     max_context_len, cache) exceeds PKV_STATIC_DECODE_WORKSPACE_BYTES the
+ *     call returns PKV_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (the kernels write every scratch entry they read, so no state carries
+ *     over).  Calls that may overlap on the GPU -- on different streams, or
+ *     from different host threads -- race on it: serialise them.
+ */
+#define PKV_STATIC_DECODE_WORKSPACE_BYTES (16u * 1024u * 1024u)
+PKV_API int pkv_paged_decode_static_workspace(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+    int32_t num_q_heads, int32_t max_context_len, float scale, void* out,
+    pkv_cache_desc cache, uint32_t* status, void* stream);
+
+/*
  * Bytes of device workspace pkv_paged_prefill_varlen needs (pure host function).
  */
 PKV_API size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,

@@ -31,7 +31,12 @@ STATUS = {v: k for k, v in PKV_STATUS_BITS.items()}
 
 C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_store",
                "pkv_paged_decode_workspace_bytes", "pkv_paged_decode",
-               "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample"]
+               "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample",
+               "pkv_paged_decode_static_workspace"]
+
+# Size of the scratch array compiled into the library for
+# pkv_paged_decode_static_workspace (PKV_STATIC_DECODE_WORKSPACE_BYTES).
+STATIC_DECODE_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
 class CacheDesc(ctypes.Structure):
@@ -234,4 +239,35 @@ def sample(logits, temperatures, exp_noise, out=None, status=None, stream=None) 
                         _dev(out, "out", torch.int32, dev),
                         _ptr_or_null(status, "status", torch.int32, dev), _stream(dev, stream))
     _check(rc, "pkv_sample")
+    return out
+
+
+def paged_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                  max_context_len, out=None, status=None,
+                                  stream=None) -> torch.Tensor:
+    """paged_decode for callers that cannot allocate device memory where they
+    call (e.g. a plugin whose host engine owns all device memory, or a loop
+    that must not pay for cudaMalloc's implicit synchronisation): the split-KV
+    scratch is the library's own fixed array of STATIC_DECODE_WORKSPACE_BYTES,
+    so apart from `out` (pass it to avoid the one allocation here) nothing is
+    allocated.  Calls share that array: do not let two of them overlap on the
+    GPU.  The first call on a device resolves the array's address; make it
+    before any stream capture."""
+    lib = load()
+    fn = lib.pkv_paged_decode_static_workspace
+    if fn.restype is not ctypes.c_int or not fn.argtypes:
+        P, I32, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+        fn.restype = ctypes.c_int
+        fn.argtypes = [P, P, P, P, I32, P, I32, I32, I32, F32, P, CacheDesc, P, P]
+    dev = k_cache.device
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = fn(_dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", torch.bfloat16, dev),
+            _dev(v_cache, "v_cache", torch.bfloat16, dev),
+            _dev(block_tables, "block_tables", torch.int32, dev), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32, dev), B, Hq, int(max_context_len),
+            float(scale), _dev(out, "out", torch.bfloat16, dev), cache_desc(k_cache),
+            _ptr_or_null(status, "status", torch.int32, dev), _stream(dev, stream))
+    _check(rc, "pkv_paged_decode_static_workspace")
     return out

@@ -485,3 +485,66 @@ extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* 
     cudaStream_t s = (cudaStream_t)stream;
     return cache.head_dim == 128 ? launch_decode<128>(a, s) : launch_decode<64>(a, s);
 }
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// For callers that cannot allocate device memory at the point of the call --
+// for example a plugin inside a host engine that owns and budgets all device
+// memory up front, or a latency-critical serving loop where cudaMalloc's
+// implicit device-wide synchronisation is unacceptable -- this variant keeps
+// the split-KV scratch in a fixed array compiled into the library.  Every GPU
+// that loads the library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[PKV_STATIC_DECODE_WORKSPACE_BYTES];
+
+// Device address of g_decode_scratch on each device.  In host code the
+// symbol's name is only a host-side handle, never a device address, so it is
+// resolved with cudaGetSymbolAddress once per device while that device is
+// current.
+void* static_scratch_for_current_device(int* err) {
+    static std::mutex mu;
+    static void* ptr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = PKV_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
+            *err = PKV_ERR_CUDA;
+            return nullptr;
+        }
+        ptr[dev] = p;
+    }
+    return ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_decode_static_workspace(
+        const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+        int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+        int32_t num_q_heads, int32_t max_context_len, float scale, void* out,
+        pkv_cache_desc cache, uint32_t* status, void* stream) {
+    if (batch < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 ||
+        cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0)
+        return PKV_ERR_BAD_DIMENSION;
+    if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_BAD_DIMENSION;
+    if (cache.head_dim != 64 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED_HEAD_DIM;
+    if (batch == 0) return PKV_OK;
+    const DecodeLayout L = decode_layout(batch, num_q_heads, max_context_len, cache);
+    if (L.total > (size_t)PKV_STATIC_DECODE_WORKSPACE_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    int err = PKV_OK;
+    void* scratch = static_scratch_for_current_device(&err);
+    if (scratch == nullptr) return err;
+    return pkv_paged_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            batch, num_q_heads, max_context_len, scale, out, scratch,
+                            (size_t)PKV_STATIC_DECODE_WORKSPACE_BYTES, cache, status, stream);
+}

@@ -1,15 +1,467 @@
-// paged_prefill_varlen fast path on the 5th-generation tensor cores
-// (tcgen05.mma with TMEM accumulators, TMA-staged Q/K/V tiles).
-#include "prefill_common.cuh"
+// paged_prefill_varlen on the 5th-generation tensor cores: tcgen05.mma with
+// TMEM accumulators, Q/K/V tiles staged by TMA, for head_dim 128 and block
+// sizes that are multiples of 128.
+//
+// What it computes is stated in prefill.cu (causal varlen prefill over a
+// prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
+//
+// Work item = (sequence, 128-query tile, q head); the persistent grid walks
+// the cost-sorted tile list of the plan kernel (heads innermost, so the G
+// heads of a kv group read the same K/V tiles out of L2 at about the same
+// time).  The keys of a q tile are covered by
+//   * cached tiles u = 0 .. ceil(c/128)-1: keys 128u .. 128u+127 of the
+//     prefix, one TMA box per half of head_dim at row
+//     block_tables[b][128u / bs] * bs + (128u % bs) of the pool (a 128-key
+//     tile never crosses a block because bs is a multiple of 128);
+//   * new tiles t = 0 .. m: the chunk's own k/v rows q0 + 128t ..; tile t == m
+//     is the diagonal (causal mask col <= row), tiles t > m are never visible.
+// Masked keys get -inf scores; V rows of masked cached keys are zeroed in
+// shared memory because unused cache slots may hold NaN.
+//
+// Roles (192 threads, one CTA per SM):
+//   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
+//              masks, keeps a running row maximum that is only raised (and O,
+//              l rescaled) when the new maximum exceeds it by more than 2^8,
+//              writes P = exp2(S - m) as bf16 into shared memory in the
+//              128-byte-swizzled K-major layout, and finally normalises O.
+//   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
+//              two-stage ring.
+//   warp 5     MMA issuer (one thread): S = Q K^T (both K-major) into one of
+//              two TMEM S buffers, then O += P V (V MN-major), with the next
+//              tile's Q K^T issued before waiting for this tile's P so the
+//              tensor pipe overlaps the softmax.  Also owns TMEM.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384) of a 512-column
+// allocation.  Every mbarrier wait is bounded; a wait that gives up sets
+// PKV_STATUS_WAIT_TIMEOUT and the CTA unwinds, waits for its own copies and
+// MMAs, and frees TMEM.
+#include <cudaTypedefs.h>
 
-int pkv_prefill_tc_supported(const pkv::PrefillArgs& a, int head_dim) {
-    (void)a;
-    (void)head_dim;
-    return PKV_ERR_UNSUPPORTED;
+#include "prefill_common.cuh"
+#include "tc_utils.cuh"
+
+using pkv::PrefillArgs;
+using namespace pkv::tc;
+
+namespace {
+
+constexpr int kBM = 128;                 // queries per tile
+constexpr int kBN = 128;                 // keys per tile
+constexpr int kD = 128;                  // head_dim
+constexpr int kTile = kBM * kD * 2;      // bytes of one bf16 128x128 tile
+constexpr int kHalf = kTile / 2;         // one 64-column half (128 rows x 128 B)
+constexpr int kThreads = 192;
+constexpr uint32_t kColS0 = 0, kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
+
+struct __align__(1024) TcSmem {
+    unsigned char q[kTile];
+    unsigned char k[2][kTile];
+    unsigned char v[2][kTile];
+    unsigned char p[kTile];
+    uint64_t q_full, q_free;
+    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full, pv_done, o_free, mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct TcMaps {
+    CUtensorMap q, k, v, kc, vc;
+};
+
+struct Item {
+    int32_t b, m, h, q0, lq, lk, c, n_cached, n_tiles, rows;
+};
+
+__device__ __forceinline__ Item item_at(const PrefillArgs& a, int64_t it) {
+    Item x;
+    const int32_t tile = (int32_t)(it / a.Hq);
+    x.h = (int32_t)(it - (int64_t)tile * a.Hq);
+    const int2 tm = a.tiles[tile];
+    x.b = tm.x;
+    x.m = tm.y;
+    x.q0 = a.cu_q[x.b];
+    x.lq = a.cu_q[x.b + 1] - x.q0;
+    x.lk = a.cu_k[x.b + 1] - a.cu_k[x.b];
+    x.c = x.lk - x.lq;
+    x.n_cached = (x.c + kBN - 1) / kBN;
+    x.n_tiles = x.n_cached + x.m + 1;
+    x.rows = min(kBM, x.lq - x.m * kBM);
+    return x;
 }
 
-int pkv_launch_prefill_tc(pkv::PrefillArgs& a, cudaStream_t s) {
-    (void)a;
-    (void)s;
-    return PKV_ERR_UNSUPPORTED;
+// All 32 lanes wait on the same barrier; the result is made warp-uniform so
+// the warp-wide TMEM instructions that follow never see a diverged warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const int* abort_flag) {
+    const bool r = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+__device__ __forceinline__ void give_up(TcSmem& s, uint32_t* status) {
+    s.abort_flag = 1;
+    pkv::report(status, PKV_STATUS_WAIT_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
+        const __grid_constant__ TcMaps maps, const PrefillArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    TcSmem& s = *reinterpret_cast<TcSmem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        s.abort_flag = 0;
+        mbar_init(&s.q_full, 1);
+        mbar_init(&s.q_free, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.k_full[i], 1);
+            mbar_init(&s.v_full[i], 1);
+            mbar_init(&s.kv_empty[i], 1);
+            mbar_init(&s.s_full[i], 1);
+            mbar_init(&s.s_free[i], 128);
+        }
+        mbar_init(&s.p_full, 128);
+        mbar_init(&s.pv_done, 1);
+        mbar_init(&s.o_free, 128);
+        mbar_init(&s.mma_done, 1);
+        mbar_init_fence();
+    }
+    if (warp == 5) tmem_alloc(&s.tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    const int64_t n_items = (int64_t)a.sched[0] * a.Hq;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.v);
+            if (a.bt) {
+                tma_prefetch_desc(&maps.kc);
+                tma_prefetch_desc(&maps.vc);
+            }
+            uint32_t T = 0, I = 0;
+            bool ok = true, bad_block = false;
+            const int32_t oob_row = a.NB * a.bs;   // past the pool: TMA fills zeros
+            for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
+                const Item x = item_at(a, it);
+                const int32_t kvh = x.h / a.G;
+                if (I > 0 && !(ok = mbar_wait(&s.q_free, (I - 1) & 1, &s.abort_flag))) break;
+                mbar_expect_tx(&s.q_full, kTile);
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
+                                x.q0 + x.m * kBM);
+                for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
+                    const int st = T & 1;
+                    const uint32_t use = T >> 1;
+                    if (use > 0 && !(ok = mbar_wait(&s.kv_empty[st], (use - 1) & 1, &s.abort_flag)))
+                        break;
+                    const CUtensorMap* mk;
+                    const CUtensorMap* mv;
+                    int32_t row;
+                    if (j < x.n_cached) {
+                        const int32_t key0 = j * kBN;
+                        const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
+                        if ((unsigned)blk < (unsigned)a.NB) {
+                            row = blk * a.bs + key0 % a.bs;
+                        } else {
+                            row = oob_row;
+                            bad_block = true;
+                        }
+                        mk = &maps.kc;
+                        mv = &maps.vc;
+                    } else {
+                        row = x.q0 + (j - x.n_cached) * kBN;
+                        mk = &maps.k;
+                        mv = &maps.v;
+                    }
+                    mbar_expect_tx(&s.k_full[st], kTile);
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(s.k[st] + hf * kHalf, mk, &s.k_full[st], hf * 64, kvh, row);
+                    mbar_expect_tx(&s.v_full[st], kTile);
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(s.v[st] + hf * kHalf, mv, &s.v_full[st], hf * 64, kvh, row);
+                }
+            }
+            if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
+            if (!ok) {
+                give_up(s, a.status);
+                // let the copies already issued land before the CTA exits
+                for (int back = 1; back <= 2 && (int)T - back >= 0; ++back) {
+                    const uint32_t t = T - back;
+                    mbar_drain(&s.k_full[t & 1], (t >> 1) & 1);
+                    mbar_drain(&s.v_full[t & 1], (t >> 1) & 1);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = umma_idesc_bf16(kBM, kBN, false);
+            const uint32_t id_pv = umma_idesc_bf16(kBM, kD, true);
+            const uint32_t q_addr = saddr(s.q), p_addr = saddr(s.p);
+            uint32_t T = 0, I = 0;
+            bool ok = true;
+            auto issue_qk = [&](uint32_t t) -> bool {
+                const int st = t & 1;
+                if (!mbar_wait(&s.k_full[st], (t >> 1) & 1, &s.abort_flag)) return false;
+                if (t >= 2 && !mbar_wait(&s.s_free[st], ((t >> 1) - 1) & 1, &s.abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint32_t k_addr = saddr(s.k[st]);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    umma_bf16(tmem + kColS0 + st * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
+                              umma_desc_sw128(k_addr + off, 16, 1024), id_qk, kk > 0);
+                }
+                umma_commit(&s.s_full[st]);
+                return true;
+            };
+            for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
+                const Item x = item_at(a, it);
+                if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag))) break;
+                tc_fence_after();
+                if (!(ok = issue_qk(T))) break;
+                for (int32_t j = 0; j < x.n_tiles; ++j) {
+                    const uint32_t t = T + j;
+                    if (j + 1 < x.n_tiles) {
+                        if (!(ok = issue_qk(t + 1))) break;
+                    } else {
+                        umma_commit(&s.q_free);          // every Q K^T of the item issued
+                    }
+                    if (!(ok = mbar_wait(&s.p_full, t & 1, &s.abort_flag))) break;
+                    if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1, &s.abort_flag)))
+                        break;
+                    const int st = t & 1;
+                    if (!(ok = mbar_wait(&s.v_full[st], (t >> 1) & 1, &s.abort_flag))) break;
+                    tc_fence_after();
+                    const uint32_t v_addr = saddr(s.v[st]);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        umma_bf16(tmem + kColO, umma_desc_sw128(p_addr + poff, 16, 1024),
+                                  umma_desc_sw128(v_addr + kk * 2048, kHalf, 1024), id_pv,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&s.pv_done);
+                    umma_commit(&s.kv_empty[st]);
+                }
+                T += x.n_tiles;
+            }
+            if (!ok) give_up(s, a.status);
+            // every MMA this thread issued has finished before TMEM is freed
+            umma_commit(&s.mma_done);
+            mbar_drain(&s.mma_done, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int i = tid;                          // query row == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        uint32_t T = 0, I = 0;
+        bool ok = true;
+        for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
+            const Item x = item_at(a, it);
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int32_t j = 0; j < x.n_tiles && ok; ++j) {
+                const uint32_t t = T + j;
+                const int sb = t & 1;
+                if (!(ok = warp_wait(&s.s_full[sb], (t >> 1) & 1, &s.abort_flag))) break;
+                tc_fence_after();
+                float sv[kBN];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    tmem_ld32(lane_base + kColS0 + sb * kBN + cc * 32, sv + cc * 32);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&s.s_free[sb]);
+                // visible keys of this tile for row i: col < lim
+                int32_t lim;
+                bool partial_cached = false;
+                if (j < x.n_cached) {
+                    lim = min(kBN, x.c - j * kBN);
+                    partial_cached = lim < kBN;
+                } else {
+                    lim = (j - x.n_cached == x.m) ? i + 1 : kBN;
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int col = 0; col < kBN; ++col) {
+                    const float v = col < lim ? sv[col] * a.scale_log2 : -INFINITY;
+                    sv[col] = v;
+                    mx = fmaxf(mx, v);
+                }
+                const bool raise = mx > m_run + kRescaleThreshold;
+                float alpha = 1.f;
+                if (raise) {
+                    alpha = (m_run == -INFINITY) ? 0.f : pkv::fast_exp2(m_run - mx);
+                    m_run = mx;
+                    l_run *= alpha;
+                }
+                // P buffer and O are free once the previous P V has finished
+                if (t > 0 && !(ok = warp_wait(&s.pv_done, (t - 1) & 1, &s.abort_flag))) break;
+                if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        float ov[32];
+                        tmem_ld32(lane_base + kColO + cc * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+                        tmem_st32(lane_base + kColO + cc * 32, ov);
+                    }
+                    tmem_wait_st();
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                float lsum = 0.f;
+                unsigned char* prow = s.p + i * 128;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int qc = 0; qc < 8; ++qc) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = hf * 64 + qc * 8 + 2 * e;
+                            const float p0 = pkv::fast_exp2(sv[col] - m_use);
+                            const float p1 = pkv::fast_exp2(sv[col + 1] - m_use);
+                            lsum += p0 + p1;
+                            w[e] = pkv::pack_bf16(p0, p1);
+                        }
+                        *reinterpret_cast<uint4*>(prow + hf * kHalf + ((qc ^ (i & 7)) * 16)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                l_run += lsum;
+                if (partial_cached) {
+                    // masked cached slots may hold NaN: zero their V rows
+                    const int st = t & 1;
+                    if (!(ok = warp_wait(&s.v_full[st], (t >> 1) & 1, &s.abort_flag))) break;
+                    if (i >= lim) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                            for (int qc = 0; qc < 8; ++qc)
+                                *reinterpret_cast<uint4*>(s.v[st] + hf * kHalf + i * 128 + qc * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&s.p_full);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l to global ----
+            const uint32_t tl = T + x.n_tiles - 1;
+            if (!(ok = warp_wait(&s.pv_done, tl & 1, &s.abort_flag))) break;
+            tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            __nv_bfloat16* orow = a.out + ((int64_t)(x.q0 + x.m * kBM + i) * a.Hq + x.h) * kD;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float ov[32];
+                tmem_ld32(lane_base + kColO + cc * 32, ov);
+                tmem_wait_ld();
+                if (i < x.rows) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 pk;
+                        pk.x = pkv::pack_bf16(ov[q4 * 8 + 0] * inv, ov[q4 * 8 + 1] * inv);
+                        pk.y = pkv::pack_bf16(ov[q4 * 8 + 2] * inv, ov[q4 * 8 + 3] * inv);
+                        pk.z = pkv::pack_bf16(ov[q4 * 8 + 4] * inv, ov[q4 * 8 + 5] * inv);
+                        pk.w = pkv::pack_bf16(ov[q4 * 8 + 6] * inv, ov[q4 * 8 + 7] * inv);
+                        *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pk;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&s.o_free);
+            T += x.n_tiles;
+        }
+        if (!ok) give_up(s, a.status);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// [rows, heads, 128] bf16 viewed as a 3-D tensor (head_dim innermost); box =
+// 64 elements (128 B, the swizzle width) x 1 head x 128 rows.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
+    if (head_dim != kD) return PKV_ERR_UNSUPPORTED;
+    if (a.bt != nullptr && (a.bs % kBN) != 0) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)a.NB * a.bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
+    if (encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s) {
+    TcMaps maps;
+    if (!encode_rows(&maps.q, a.q, a.total_q, a.Hq) ||
+        !encode_rows(&maps.k, a.k, a.total_q, a.Hkv) ||
+        !encode_rows(&maps.v, a.v, a.total_q, a.Hkv))
+        return PKV_ERR_CUDA;
+    if (a.bt) {
+        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv) ||
+            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv))
+            return PKV_ERR_CUDA;
+    } else {
+        maps.kc = maps.k;
+        maps.vc = maps.v;
+    }
+    a.tile_m = kBM;
+    a.tile_n = kBN;
+    int rc = pkv_launch_prefill_plan(a, s);
+    if (rc != PKV_OK) return rc;
+    const int smem = (int)sizeof(TcSmem) + 1024;
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured = true;
+    }
+    int64_t grid = pkv_num_sms();
+    const int64_t upper = (int64_t)a.max_tiles * a.Hq;
+    if (grid > upper) grid = upper;
+    if (grid < 1) grid = 1;
+    prefill_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(maps, a);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -22,10 +22,11 @@
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks, keeps a running row maximum that is only raised (and O,
 //              l rescaled) when the new maximum exceeds it by more than 2^8,
-//              writes P = exp2(S - m) as bf16 into shared memory in the
-//              128-byte-swizzled K-major layout, and finally normalises O.
+//              writes P = exp2(S - m) as bf16 in the 128-byte-swizzled K-major
+//              layout into the K buffer of the same stage (free once S = Q K^T
+//              has completed, and the same size), and finally normalises O.
 //   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
-//              two-stage ring.
+//              three-stage ring.
 //   warp 5     MMA issuer (one thread): S = Q K^T (both K-major) into one of
 //              two TMEM S buffers, then O += P V (V MN-major), with the next
 //              tile's Q K^T issued before waiting for this tile's P so the
@@ -50,18 +51,18 @@ constexpr int kD = 128;                  // head_dim
 constexpr int kTile = kBM * kD * 2;      // bytes of one bf16 128x128 tile
 constexpr int kHalf = kTile / 2;         // one 64-column half (128 rows x 128 B)
 constexpr int kThreads = 192;
+constexpr int kStages = 3;               // K/V ring depth
 constexpr uint32_t kColS0 = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
 
 struct __align__(1024) TcSmem {
     unsigned char q[kTile];
-    unsigned char k[2][kTile];
-    unsigned char v[2][kTile];
-    unsigned char p[kTile];
+    unsigned char k[kStages][kTile];     // K tile, then P of the same tile
+    unsigned char v[kStages][kTile];
     uint64_t q_full, q_free;
-    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], p_full[kStages];
     uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done, o_free, mma_done;
+    uint64_t pv_done, o_free, mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -113,14 +114,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         s.abort_flag = 0;
         mbar_init(&s.q_full, 1);
         mbar_init(&s.q_free, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.v_full[i], 1);
             mbar_init(&s.kv_empty[i], 1);
+            mbar_init(&s.p_full[i], 128);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s.s_full[i], 1);
             mbar_init(&s.s_free[i], 128);
         }
-        mbar_init(&s.p_full, 128);
         mbar_init(&s.pv_done, 1);
         mbar_init(&s.o_free, 128);
         mbar_init(&s.mma_done, 1);
@@ -155,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
                                 x.q0 + x.m * kBM);
                 for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
-                    const int st = T & 1;
-                    const uint32_t use = T >> 1;
+                    const int st = T % kStages;
+                    const uint32_t use = T / kStages;
                     if (use > 0 && !(ok = mbar_wait(&s.kv_empty[st], (use - 1) & 1, &s.abort_flag)))
                         break;
                     const CUtensorMap* mk;
@@ -190,10 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             if (!ok) {
                 give_up(s, a.status);
                 // let the copies already issued land before the CTA exits
-                for (int back = 1; back <= 2 && (int)T - back >= 0; ++back) {
+                for (int back = 1; back <= kStages && (int)T - back >= 0; ++back) {
                     const uint32_t t = T - back;
-                    mbar_drain(&s.k_full[t & 1], (t >> 1) & 1);
-                    mbar_drain(&s.v_full[t & 1], (t >> 1) & 1);
+                    mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
+                    mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
                 }
             }
         }
@@ -202,23 +205,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         if (lane == 0) {
             const uint32_t id_qk = umma_idesc_bf16(kBM, kBN, false);
             const uint32_t id_pv = umma_idesc_bf16(kBM, kD, true);
-            const uint32_t q_addr = saddr(s.q), p_addr = saddr(s.p);
+            const uint32_t q_addr = saddr(s.q);
             uint32_t T = 0, I = 0;
             bool ok = true;
             auto issue_qk = [&](uint32_t t) -> bool {
-                const int st = t & 1;
-                if (!mbar_wait(&s.k_full[st], (t >> 1) & 1, &s.abort_flag)) return false;
-                if (t >= 2 && !mbar_wait(&s.s_free[st], ((t >> 1) - 1) & 1, &s.abort_flag))
+                const int st = t % kStages, sb = t & 1;
+                if (!mbar_wait(&s.k_full[st], (t / kStages) & 1, &s.abort_flag)) return false;
+                if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t >> 1) - 1) & 1, &s.abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t k_addr = saddr(s.k[st]);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma_bf16(tmem + kColS0 + st * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
+                    umma_bf16(tmem + kColS0 + sb * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
                               umma_desc_sw128(k_addr + off, 16, 1024), id_qk, kk > 0);
                 }
-                umma_commit(&s.s_full[st]);
+                umma_commit(&s.s_full[sb]);
                 return true;
             };
             for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
@@ -233,13 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     } else {
                         umma_commit(&s.q_free);          // every Q K^T of the item issued
                     }
-                    if (!(ok = mbar_wait(&s.p_full, t & 1, &s.abort_flag))) break;
+                    const int st = t % kStages;
+                    if (!(ok = mbar_wait(&s.p_full[st], (t / kStages) & 1, &s.abort_flag))) break;
                     if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1, &s.abort_flag)))
                         break;
-                    const int st = t & 1;
-                    if (!(ok = mbar_wait(&s.v_full[st], (t >> 1) & 1, &s.abort_flag))) break;
+                    if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
                     tc_fence_after();
                     const uint32_t v_addr = saddr(s.v[st]);
+                    const uint32_t p_addr = saddr(s.k[st]);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
                         const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -301,9 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     m_run = mx;
                     l_run *= alpha;
                 }
-                // P buffer and O are free once the previous P V has finished
-                if (t > 0 && !(ok = warp_wait(&s.pv_done, (t - 1) & 1, &s.abort_flag))) break;
+                const int st = t % kStages;
                 if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                    // O may only be rescaled once the previous P V has finished
+                    // (the one before it is, since S of this tile was committed
+                    // after it, so this parity wait is unambiguous)
+                    if (!(ok = warp_wait(&s.pv_done, (t - 1) & 1, &s.abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
@@ -318,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 }
                 const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
                 float lsum = 0.f;
-                unsigned char* prow = s.p + i * 128;
+                unsigned char* prow = s.k[st] + i * 128;   // Q K^T of this tile is done
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -339,8 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 l_run += lsum;
                 if (partial_cached) {
                     // masked cached slots may hold NaN: zero their V rows
-                    const int st = t & 1;
-                    if (!(ok = warp_wait(&s.v_full[st], (t >> 1) & 1, &s.abort_flag))) break;
+                    if (!(ok = warp_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
                     if (i >= lim) {
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf)
@@ -352,11 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&s.p_full);
+                mbar_arrive(&s.p_full[st]);
             }
             if (!ok) break;
             // ---- epilogue: O / l to global ----
+            // pv_done completes once per tile.  S of the last tile was committed
+            // after P V of the tile two before it, so that one is complete; wait
+            // for the previous tile's and then the last tile's in order, so the
+            // parity of each wait is unambiguous.
             const uint32_t tl = T + x.n_tiles - 1;
+            if (tl > 0 && !(ok = warp_wait(&s.pv_done, (tl - 1) & 1, &s.abort_flag))) break;
             if (!(ok = warp_wait(&s.pv_done, tl & 1, &s.abort_flag))) break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;

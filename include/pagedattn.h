@@ -203,6 +203,7 @@ PKV_API size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,
  *   max_seqlen_q/k host upper bounds of Lq/Lk
  *   block_tables  device [batch, max_blocks_per_seq] int32, or NULL when no
  *                 sequence has a cached prefix (then Lk must equal Lq)
+ *   scale         softmax scale, positive and finite (e.g. 1/sqrt(head_dim))
  *   out           device, [total_q, num_q_heads, head_dim] bf16
  *   workspace     device, >= pkv_paged_prefill_workspace_bytes(...) bytes,
  *                 16-byte aligned; holds the tile schedule

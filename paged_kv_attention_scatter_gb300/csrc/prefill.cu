@@ -403,6 +403,7 @@ extern "C" int pkv_paged_prefill_varlen(
         max_seqlen_q < 0 || max_seqlen_k < 0)
         return PKV_ERR_BAD_DIMENSION;
     if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_BAD_DIMENSION;
+    if (!(scale > 0.f) || !isfinite(scale)) return PKV_ERR_BAD_DIMENSION;
     if (cache.head_dim != 64 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED_HEAD_DIM;
     if (block_tables && (max_blocks_per_seq <= 0 || cache.num_blocks <= 0 ||
                          cache.block_size <= 0))

@@ -20,19 +20,23 @@
 //
 // Roles (192 threads, one CTA per SM):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
-//              masks, keeps a running row maximum that is only raised (and O,
-//              l rescaled) when the new maximum exceeds it by more than 2^8,
-//              writes P = exp2(S - m) as bf16 in the 128-byte-swizzled K-major
-//              layout into the K buffer of the same stage (free once S = Q K^T
-//              has completed, and the same size), and finally normalises O.
+//              masks (diagonal and partial tiles only), keeps a running row
+//              maximum that is only raised (and O, l rescaled) when the new
+//              maximum exceeds it by more than 2^8, and stores P = exp2(S - m)
+//              as packed bf16 back into the first 64 columns of the same S
+//              buffer; at the end it normalises O.
 //   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
 //              three-stage ring.
-//   warp 5     MMA issuer (one thread): S = Q K^T (both K-major) into one of
-//              two TMEM S buffers, then O += P V (V MN-major), with the next
-//              tile's Q K^T issued before waiting for this tile's P so the
-//              tensor pipe overlaps the softmax.  Also owns TMEM.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384) of a 512-column
-// allocation.  Every mbarrier wait is bounded; a wait that gives up sets
+//   warp 5     MMA issuer (one thread): S = Q K^T (both operands K-major in
+//              shared memory) into one of three TMEM S buffers, then
+//              O += P V with P read from TMEM and V MN-major in shared memory.
+//              The next tile's Q K^T is issued before waiting for this tile's
+//              P, so the tensor pipe overlaps the softmax; Q K^T into a buffer
+//              waits for the P V that last read P from it.  Also owns TMEM.
+// Keeping P in TMEM means shared memory only carries Q, K and V: an SS MMA of
+// 128x128x16 already reads 128 bytes per clock from it.
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512); stage,
+// S buffer and the barriers of tile t all use index t % 3.  Every mbarrier wait is bounded; a wait that gives up sets
 // PKV_STATUS_WAIT_TIMEOUT and the CTA unwinds, waits for its own copies and
 // MMAs, and frees TMEM.
 #include <cudaTypedefs.h>
@@ -52,17 +56,17 @@ constexpr int kTile = kBM * kD * 2;      // bytes of one bf16 128x128 tile
 constexpr int kHalf = kTile / 2;         // one 64-column half (128 rows x 128 B)
 constexpr int kThreads = 192;
 constexpr int kStages = 3;               // K/V ring depth
-constexpr uint32_t kColS0 = 0, kColO = 256;
+constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
 
 struct __align__(1024) TcSmem {
     unsigned char q[kTile];
-    unsigned char k[kStages][kTile];     // K tile, then P of the same tile
+    unsigned char k[kStages][kTile];
     unsigned char v[kStages][kTile];
     uint64_t q_full, q_free;
-    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages], p_full[kStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t pv_done, o_free, mma_done;
+    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t s_full[kStages], p_full[kStages], pv_done[kStages];
+    uint64_t o_free, mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -118,13 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.v_full[i], 1);
             mbar_init(&s.kv_empty[i], 1);
-            mbar_init(&s.p_full[i], 128);
-        }
-        for (int i = 0; i < 2; ++i) {
             mbar_init(&s.s_full[i], 1);
-            mbar_init(&s.s_free[i], 128);
+            mbar_init(&s.p_full[i], 128);
+            mbar_init(&s.pv_done[i], 1);
         }
-        mbar_init(&s.pv_done, 1);
         mbar_init(&s.o_free, 128);
         mbar_init(&s.mma_done, 1);
         mbar_init_fence();
@@ -209,19 +210,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             uint32_t T = 0, I = 0;
             bool ok = true;
             auto issue_qk = [&](uint32_t t) -> bool {
-                const int st = t % kStages, sb = t & 1;
+                const int st = t % kStages;
                 if (!mbar_wait(&s.k_full[st], (t / kStages) & 1, &s.abort_flag)) return false;
-                if (t >= 2 && !mbar_wait(&s.s_free[sb], ((t >> 1) - 1) & 1, &s.abort_flag))
+                // the S buffer still holds P of tile t-3 until its P V is done
+                if (t >= kStages &&
+                    !mbar_wait(&s.pv_done[st], (t / kStages - 1) & 1, &s.abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t k_addr = saddr(s.k[st]);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma_bf16(tmem + kColS0 + sb * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
+                    umma_bf16(tmem + kColS0 + st * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
                               umma_desc_sw128(k_addr + off, 16, 1024), id_qk, kk > 0);
                 }
-                umma_commit(&s.s_full[sb]);
+                umma_commit(&s.s_full[st]);
                 return true;
             };
             for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
@@ -243,15 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
                     tc_fence_after();
                     const uint32_t v_addr = saddr(s.v[st]);
-                    const uint32_t p_addr = saddr(s.k[st]);
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        umma_bf16(tmem + kColO, umma_desc_sw128(p_addr + poff, 16, 1024),
-                                  umma_desc_sw128(v_addr + kk * 2048, kHalf, 1024), id_pv,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&s.pv_done);
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_bf16_tmem_a(tmem + kColO, tmem + kColS0 + st * kBN + kk * 8,
+                                         umma_desc_sw128(v_addr + kk * 2048, kHalf, 1024), id_pv,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&s.pv_done[st]);
                     umma_commit(&s.kv_empty[st]);
                 }
                 T += x.n_tiles;
@@ -272,32 +272,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             float m_run = -INFINITY, l_run = 0.f;
             for (int32_t j = 0; j < x.n_tiles && ok; ++j) {
                 const uint32_t t = T + j;
-                const int sb = t & 1;
-                if (!(ok = warp_wait(&s.s_full[sb], (t >> 1) & 1, &s.abort_flag))) break;
+                const int st = t % kStages;
+                const uint32_t s_col = lane_base + kColS0 + st * kBN;
+                if (!(ok = warp_wait(&s.s_full[st], (t / kStages) & 1, &s.abort_flag))) break;
                 tc_fence_after();
                 float sv[kBN];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    tmem_ld32(lane_base + kColS0 + sb * kBN + cc * 32, sv + cc * 32);
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(s_col + cc * 32, sv + cc * 32);
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&s.s_free[sb]);
                 // visible keys of this tile for row i: col < lim
-                int32_t lim;
-                bool partial_cached = false;
+                int32_t lim = kBN;
+                bool partial_cached = false, masked = false;
                 if (j < x.n_cached) {
                     lim = min(kBN, x.c - j * kBN);
-                    partial_cached = lim < kBN;
-                } else {
-                    lim = (j - x.n_cached == x.m) ? i + 1 : kBN;
+                    partial_cached = masked = lim < kBN;
+                } else if (j - x.n_cached == x.m) {
+                    lim = i + 1;
+                    masked = true;
                 }
                 float mx = -INFINITY;
+                if (masked) {
 #pragma unroll
-                for (int col = 0; col < kBN; ++col) {
-                    const float v = col < lim ? sv[col] * a.scale_log2 : -INFINITY;
-                    sv[col] = v;
-                    mx = fmaxf(mx, v);
+                    for (int col = 0; col < kBN; ++col) {
+                        sv[col] = col < lim ? sv[col] : -INFINITY;
+                        mx = fmaxf(mx, sv[col]);
+                    }
+                } else {
+#pragma unroll
+                    for (int col = 0; col < kBN; ++col) mx = fmaxf(mx, sv[col]);
                 }
+                mx *= a.scale_log2;                         // scale > 0 keeps the order
                 const bool raise = mx > m_run + kRescaleThreshold;
                 float alpha = 1.f;
                 if (raise) {
@@ -305,12 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     m_run = mx;
                     l_run *= alpha;
                 }
-                const int st = t % kStages;
                 if (j > 0 && __any_sync(0xffffffffu, raise)) {
                     // O may only be rescaled once the previous P V has finished
-                    // (the one before it is, since S of this tile was committed
-                    // after it, so this parity wait is unambiguous)
-                    if (!(ok = warp_wait(&s.pv_done, (t - 1) & 1, &s.abort_flag))) break;
+                    const uint32_t tp = t - 1;
+                    if (!(ok = warp_wait(&s.pv_done[tp % kStages], (tp / kStages) & 1,
+                                         &s.abort_flag)))
+                        break;
                     tc_fence_after();
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
@@ -321,29 +325,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         for (int e = 0; e < 32; ++e) ov[e] *= alpha;
                         tmem_st32(lane_base + kColO + cc * 32, ov);
                     }
-                    tmem_wait_st();
                 }
-                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
                 float lsum = 0.f;
-                unsigned char* prow = s.k[st] + i * 128;   // Q K^T of this tile is done
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
+                for (int half = 0; half < 2; ++half) {
+                    float pw[32];                               // packed bf16 pairs
 #pragma unroll
-                    for (int qc = 0; qc < 8; ++qc) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int col = hf * 64 + qc * 8 + 2 * e;
-                            const float p0 = pkv::fast_exp2(sv[col] - m_use);
-                            const float p1 = pkv::fast_exp2(sv[col + 1] - m_use);
-                            lsum += p0 + p1;
-                            w[e] = pkv::pack_bf16(p0, p1);
-                        }
-                        *reinterpret_cast<uint4*>(prow + hf * kHalf + ((qc ^ (i & 7)) * 16)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int e = 0; e < 32; ++e) {
+                        const int col = half * 64 + 2 * e;
+                        const float p0 = pkv::fast_exp2(fmaf(sv[col], a.scale_log2, neg_m));
+                        const float p1 = pkv::fast_exp2(fmaf(sv[col + 1], a.scale_log2, neg_m));
+                        lsum += p0 + p1;
+                        pw[e] = __uint_as_float(pkv::pack_bf16(p0, p1));
                     }
+                    tmem_st32(s_col + half * 32, pw);           // P aliases S columns 0..63
                 }
                 l_run += lsum;
+                tmem_wait_st();
                 if (partial_cached) {
                     // masked cached slots may hold NaN: zero their V rows
                     if (!(ok = warp_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
@@ -355,20 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                                 *reinterpret_cast<uint4*>(s.v[st] + hf * kHalf + i * 128 + qc * 16) =
                                     make_uint4(0, 0, 0, 0);
                     }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&s.p_full[st]);
             }
             if (!ok) break;
             // ---- epilogue: O / l to global ----
-            // pv_done completes once per tile.  S of the last tile was committed
-            // after P V of the tile two before it, so that one is complete; wait
-            // for the previous tile's and then the last tile's in order, so the
-            // parity of each wait is unambiguous.
             const uint32_t tl = T + x.n_tiles - 1;
-            if (tl > 0 && !(ok = warp_wait(&s.pv_done, (tl - 1) & 1, &s.abort_flag))) break;
-            if (!(ok = warp_wait(&s.pv_done, tl & 1, &s.abort_flag))) break;
+            if (!(ok = warp_wait(&s.pv_done[tl % kStages], (tl / kStages) & 1, &s.abort_flag)))
+                break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             __nv_bfloat16* orow = a.out + ((int64_t)(x.q0 + x.m * kBM + i) * a.Hq + x.h) * kD;

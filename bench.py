@@ -265,7 +265,18 @@ def run_secondary(args, pkv, W, torch, dev, pk):
     res = {}
     flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
 
-    # ---------------- prefill-8b: chunked, prefix-cached ----------------
+    which = set(args.secondary.split(",")) if args.secondary else set()
+    if "prefill" in which:
+        res.update(bench_prefill(pkv, W, torch, dev, pk, flush))
+    if "decode32" in which:
+        res.update(bench_decode32(pkv, W, torch, dev, pk))
+    if "step" in which:
+        res.update(bench_step(pkv, W, torch, dev, pk))
+    return res
+
+
+def bench_prefill(pkv, W, torch, dev, pk, flush):
+    res = {}
     spec = W.PREFILL_8B
     w = W.prefill_workload(spec)
     kc, vc = w.k_cache0.to(dev), w.v_cache0.to(dev)
@@ -325,8 +336,11 @@ def run_secondary(args, pkv, W, torch, dev, pk):
                   "before each step, mean of 3 passes"}
     del steps, kc, vc, w
     torch.cuda.empty_cache()
+    return res
 
-    # ---------------- decode-32b: skewed long contexts ----------------
+
+def bench_decode32(pkv, W, torch, dev, pk):
+    res = {}
     for spec, key in ((W.DECODE_32B, "decode-32b"),):
         w = W.decode_workload(spec, device=dev)
         bt, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
@@ -347,8 +361,11 @@ def run_secondary(args, pkv, W, torch, dev, pk):
                     "bytes": nbytes}
         del w, g, out, ws
         torch.cuda.empty_cache()
+    return res
 
-    # ---------------- step-8b: store + decode + sample ----------------
+
+def bench_step(pkv, W, torch, dev, pk):
+    res = {}
     spec = W.STEP_8B
     w = W.decode_workload(spec, device=dev)
     bt, ctx, sl = w.block_tables.to(dev), w.context_lens.to(dev), w.slot_mapping.to(dev)
@@ -448,6 +465,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--secondary", default="prefill,decode32,step",
+                    help="comma list of secondary workloads: prefill, decode32, step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-worker", action="store_true")
     ap.add_argument("--per-step", type=int, default=1)

@@ -30,6 +30,12 @@
 //    CTA merge through shared memory; units of a sequence with more than one
 //    chunk write (m, l, unnormalised o) to the workspace and a combine kernel
 //    merges them.  A sequence with a single chunk is written directly.
+//  * plan -> split -> combine are chained as programmatic dependent launches:
+//    each kernel lets the next one launch as soon as it starts, and the next
+//    one waits (griddepcontrol.wait) for its predecessor's results, so launch
+//    latency is hidden.  (Folding the combine into the split kernel with
+//    per-group tickets was measured slower: the ticket round trip per unit
+//    stalls the K/V stream.)
 //  * Keys past ctx_b are never loaded (their registers are zero and their
 //    scores -inf), so NaN in unused cache slots cannot reach the output.
 #include "common.cuh"
@@ -65,7 +71,15 @@ __device__ __forceinline__ uint32_t pair(const uint4& a, const uint4& b, int e) 
     return __byte_perm(word(a, e >> 1), word(b, e >> 1), (e & 1) ? 0x7632 : 0x5410);
 }
 
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_predecessor() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
+    allow_dependent_launch();
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry;
     if (threadIdx.x == 0) carry = 0;
@@ -122,6 +136,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
+    allow_dependent_launch();
+    wait_for_predecessor();                  // the plan kernel's prefix sums
     const int units_per_sc = a.Hkv * a.n_hg;
     const int32_t total_sc = a.chunk_prefix[a.B];
     const int64_t units = (int64_t)total_sc * units_per_sc;
@@ -333,8 +349,17 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     }
 }
 
+constexpr int kCombineChunks = 256;  // chunks whose factors are staged at once
+
+// One CTA per (sequence, q head), one thread per head_dim element.  The
+// chunks' (max, sum) pairs and scale factors go through shared memory, so the
+// partial outputs are read with independent loads.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
+    __shared__ float f[kCombineChunks];
+    __shared__ float red[D / 32];
+    __shared__ float M_s, L_s;
+    wait_for_predecessor();                  // the split kernel's partials
     const int32_t h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
     if (n == 1) return;                                  // written by the split kernel
@@ -343,18 +368,66 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
         a.out[qh * D + d] = __float2bfloat16_rn(0.f);
         return;
     }
+    const int lane = d & 31, w = d >> 5;
+    // block max of the chunks' maxima
     float M = -INFINITY;
-    for (int c = 0; c < n; ++c) M = fmaxf(M, a.part_ml[(int64_t)(p0 + c) * a.Hq + h].x);
+    for (int c = d; c < n; c += D) M = fmaxf(M, a.part_ml[(int64_t)(p0 + c) * a.Hq + h].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red[w] = M;
+    __syncthreads();
+    if (d == 0) {
+        float m = red[0];
+        for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
+        M_s = m;
+    }
+    __syncthreads();
+    M = M_s;
     float L = 0.f, O = 0.f;
-    for (int c = 0; c < n; ++c) {
-        const int64_t slot = (int64_t)(p0 + c) * a.Hq + h;
-        const float2 ml = a.part_ml[slot];
-        if (ml.x == -INFINITY) continue;
-        const float f = pkv::fast_exp2(ml.x - M);
-        L += ml.y * f;
-        O += a.part_o[slot * D + d] * f;
+    for (int c0 = 0; c0 < n; c0 += kCombineChunks) {
+        const int cn = min(kCombineChunks, n - c0);
+        float lpart = 0.f;
+        for (int c = d; c < cn; c += D) {
+            const float2 ml = a.part_ml[(int64_t)(p0 + c0 + c) * a.Hq + h];
+            const float fc = (ml.x == -INFINITY) ? 0.f : pkv::fast_exp2(ml.x - M);
+            f[c] = fc;
+            lpart += ml.y * fc;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
+        __syncthreads();
+        if (lane == 0) red[w] = lpart;
+        __syncthreads();
+        if (d == 0) {
+            float sum = 0.f;
+            for (int i = 0; i < D / 32; ++i) sum += red[i];
+            L_s = sum;
+        }
+        __syncthreads();
+        L += L_s;
+        const float* po = a.part_o + ((int64_t)(p0 + c0) * a.Hq + h) * D + d;
+        const int64_t step = (int64_t)a.Hq * D;
+#pragma unroll 8
+        for (int c = 0; c < cn; ++c) O += f[c] * po[c * step];
+        __syncthreads();
     }
     a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+}
+
+template <typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, cudaStream_t s,
+                             Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Keys per work unit: a multiple of 64 (4 warps x 16), chosen from the sizes
@@ -416,13 +489,17 @@ int launch_decode(DecodeArgs& a, cudaStream_t s) {
     int64_t grid = (int64_t)pkv_num_sms() * per_sm;
     if (grid > upper) grid = upper;
     if (grid < 1) grid = 1;
-    decode_split_kernel<D><<<(unsigned)grid, kThreads, 0, s>>>(a);
+    if (launch_dependent(decode_split_kernel<D>, dim3((unsigned)grid), dim3(kThreads), s, a) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
     for (int32_t b0 = 0; b0 < a.B; b0 += 65535) {
         DecodeArgs sub = a;
         const int32_t rows = a.B - b0 < 65535 ? a.B - b0 : 65535;
         sub.chunk_prefix = a.chunk_prefix + b0;
         sub.out = a.out + (int64_t)b0 * a.Hq * D;
-        decode_combine_kernel<D><<<dim3((unsigned)a.Hq, (unsigned)rows), D, 0, s>>>(sub);
+        if (launch_dependent(decode_combine_kernel<D>, dim3((unsigned)a.Hq, (unsigned)rows),
+                             dim3(D), s, sub) != cudaSuccess)
+            return PKV_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

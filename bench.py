@@ -148,6 +148,24 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def slowest_rank_seconds(step_s: float, dist, device=None) -> float:
+    """The largest per-step time over all ranks (each rank is a replica; the
+    job is as fast as its slowest GPU).  Works with NCCL (CUDA device) and
+    gloo (CPU) process groups; returns step_s unchanged without one."""
+    if dist is None:
+        return step_s
+    import torch
+    t = torch.tensor([step_s], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world: int, step_s: float) -> float:
+    """Whole-job throughput of `world` identical replicas: units of all ranks
+    over the slowest rank's time."""
+    return units_per_rank * world / step_s
+
+
 # ----------------------------------------------------------------------------
 def run_ours(args, rank, world, dist):
     import torch
@@ -192,12 +210,8 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    step_s = t0.elapsed_time(t1) * 1e-3 / args.steps
-    if dist is not None:
-        t = torch.tensor([step_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_s = float(t.item())
-    value = nbytes * world / step_s / 1e9
+    step_s = slowest_rank_seconds(t0.elapsed_time(t1) * 1e-3 / args.steps, dist, dev)
+    value = replica_throughput(nbytes, world, step_s) / 1e9
 
     # ---------------- e2e through the C ABI with host buffers ----------------
     q_h = w.q.cpu().pin_memory()

@@ -28,26 +28,32 @@ namespace {
 constexpr int kBins = 4096;
 
 // One CTA: the (sequence, q tile) list ordered by decreasing number of key
-// tiles (a counting sort), so the longest tiles start first.
+// tiles (a counting sort), so the longest tiles start first.  A warp takes a
+// sequence, its lanes the sequence's q tiles.  The main kernel is launched as
+// a programmatic dependent and waits for this grid before reading the list.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int32_t hist[kBins];
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t total;
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) total = 0;
     __syncthreads();
-    for (int32_t b = threadIdx.x; b < a.B; b += blockDim.x) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    for (int32_t b = w; b < a.B; b += nwarps) {
         int32_t q0, lq, lk;
-        if (!pkv::seq_lengths(a, b, q0, lq, lk, true)) continue;
-        if (lq > a.max_sq || lk > a.max_sk) pkv::report(a.status, PKV_STATUS_BAD_SEQLENS);
+        if (!pkv::seq_lengths(a, b, q0, lq, lk, lane == 0)) continue;
+        if (lane == 0 && (lq > a.max_sq || lk > a.max_sk))
+            pkv::report(a.status, PKV_STATUS_BAD_SEQLENS);
         const int32_t c = lk - lq;
         const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
-        for (int32_t m = 0; m < nt; ++m) {
+        for (int32_t m = lane; m < nt; m += 32) {
             const int32_t lim = min(lk, c + (m + 1) * a.tile_m);
             const int32_t cost = min((lim + a.tile_n - 1) / a.tile_n, kBins - 1);
             atomicAdd(&hist[kBins - 1 - cost], 1);
         }
-        atomicAdd(&total, nt);
+        if (lane == 0) atomicAdd(&total, nt);
     }
     __syncthreads();
     // exclusive scan of hist: 4 bins per thread
@@ -60,7 +66,6 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
         sum += local[i];
     }
     int32_t x = sum;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
@@ -86,12 +91,12 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
     }
     __syncthreads();
     bool overflow = false;
-    for (int32_t b = threadIdx.x; b < a.B; b += blockDim.x) {
+    for (int32_t b = w; b < a.B; b += nwarps) {
         int32_t q0, lq, lk;
         if (!pkv::seq_lengths(a, b, q0, lq, lk, false)) continue;
         const int32_t c = lk - lq;
         const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
-        for (int32_t m = 0; m < nt; ++m) {
+        for (int32_t m = lane; m < nt; m += 32) {
             const int32_t lim = min(lk, c + (m + 1) * a.tile_m);
             const int32_t cost = min((lim + a.tile_n - 1) / a.tile_n, kBins - 1);
             const int32_t pos = atomicAdd(&hist[kBins - 1 - cost], 1);
@@ -154,6 +159,7 @@ __global__ void __launch_bounds__(kThreadsG) prefill_general_kernel(PrefillArgs 
     uint4* sK = sQ + kBM * CH;
     uint4* sV = sK + 2 * kBN * CH;
 
+    asm volatile("griddepcontrol.wait;" ::: "memory");    // the plan's tile list
     const int h = blockIdx.x;
     const int32_t slot = slot_base + (int32_t)blockIdx.y;
     if (slot >= a.sched[0]) return;
@@ -356,8 +362,18 @@ int launch_general(PrefillArgs& a, cudaStream_t s) {
     }
     for (int32_t base = 0; base < a.max_tiles; base += 65535) {
         const int32_t n = a.max_tiles - base < 65535 ? a.max_tiles - base : 65535;
-        prefill_general_kernel<D><<<dim3((unsigned)a.Hq, (unsigned)n), kThreadsG, smem, s>>>(
-            a, base);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)a.Hq, (unsigned)n, 1);
+        cfg.blockDim = dim3(kThreadsG, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, prefill_general_kernel<D>, a, base) != cudaSuccess)
+            return PKV_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
+    asm volatile("griddepcontrol.wait;" ::: "memory");    // the plan's tile list
     const int64_t n_items = (int64_t)a.sched[0] * a.Hq;
 
     if (warp == 4) {
@@ -468,6 +469,16 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s) {
     const int64_t upper = (int64_t)a.max_tiles * a.Hq;
     if (grid > upper) grid = upper;
     if (grid < 1) grid = 1;
-    prefill_tc_kernel<<<(unsigned)grid, kThreads, smem, s>>>(maps, a);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, prefill_tc_kernel, maps, a) != cudaSuccess) return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -286,7 +286,56 @@ def run_secondary(args, pkv, W, torch, dev, pk):
         res.update(bench_decode32(pkv, W, torch, dev, pk))
     if "step" in which:
         res.update(bench_step(pkv, W, torch, dev, pk))
+    if "sample" in which:
+        res.update(bench_sample(pkv, W, torch, dev, pk))
+    if "kvstore" in which:
+        res.update(bench_kvstore(pkv, W, torch, dev, pk, flush))
     return res
+
+
+def bench_sample(pkv, W, torch, dev, pk):
+    """The step-8b sampler alone: B=512 rows over a 151936-entry vocabulary."""
+    spec = W.STEP_8B
+    g = torch.Generator().manual_seed(spec.seed)
+    lg, tp, en = W.sampler_inputs(spec.batch, spec.vocab, spec.logit_sigma, spec.logit_spikes,
+                                  spec.t_lo, spec.t_hi, g)
+    lg, tp, en = lg.to(dev), tp.to(dev), en.to(dev)
+    ids = torch.empty(spec.batch, dtype=torch.int32, device=dev)
+    gm = graph_of(lambda: pkv.sample(lg, tp, en, out=ids), torch)
+    for _ in range(3):
+        gm.replay()
+    t = time_graph(gm, 50, torch)
+    b = 8.0 * spec.batch * spec.vocab + 8 * spec.batch
+    return {"sample": {"workload": f"B={spec.batch} V={spec.vocab}", "us": round(t * 1e6, 2),
+                       "gbs": round(b / t / 1e9, 1), "frac_hbm": round(b / t / 1e9 / pk["hbm"], 4),
+                       "bytes": b, "timing": "CUDA graph replays (inputs 622 MB > L2)"}}
+
+
+def bench_kvstore(pkv, W, torch, dev, pk, flush):
+    """kv_store of one 16384-token prefill chunk (rows of 8x128 bf16) into the
+    prefill-8b pool."""
+    w = W.prefill_workload(W.PREFILL_8B)
+    st = w.steps[0]
+    kc, vc = w.k_cache0.to(dev), w.v_cache0.to(dev)
+    k, v, sl = st.k.to(dev), st.v.to(dev), st.slot_mapping.to(dev)
+    for _ in range(3):
+        pkv.kv_store(k, v, kc, vc, sl)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    reps = 20
+    for _ in range(reps):
+        flush_l2(flush)
+        e0.record()
+        pkv.kv_store(k, v, kc, vc, sl)
+        e1.record()
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1) * 1e-3
+    t = tot / reps
+    b = 4.0 * k.numel() * 2
+    return {"kv_store": {"workload": f"{k.shape[0]} rows of {k.shape[1]}x{k.shape[2]} bf16",
+                         "us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1),
+                         "frac_hbm": round(b / t / 1e9 / pk["hbm"], 4), "bytes": b,
+                         "timing": "CUDA events per call, L2 flushed before each"}}
 
 
 def bench_prefill(pkv, W, torch, dev, pk, flush):
@@ -480,7 +529,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--secondary", default="prefill,decode32,step",
-                    help="comma list of secondary workloads: prefill, decode32, step")
+                    help="comma list of secondary workloads: prefill, decode32, step, "
+                         "sample, kvstore")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-worker", action="store_true")
     ap.add_argument("--per-step", type=int, default=1)

@@ -351,16 +351,29 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
 
 constexpr int kCombineChunks = 256;  // chunks whose factors are staged at once
 
-// One CTA per (sequence, q head), one thread per head_dim element.  The
-// chunks' (max, sum) pairs and scale factors go through shared memory, so the
-// partial outputs are read with independent loads.
+constexpr int kCombineHeads = 4;     // q heads per combine CTA
+
+// Barrier of the D threads of one head slice (threadIdx.y) of a combine CTA.
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
-    __shared__ float f[kCombineChunks];
-    __shared__ float red[D / 32];
-    __shared__ float M_s, L_s;
+__device__ __forceinline__ void slice_sync() {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + (int)threadIdx.y), "n"(D) : "memory");
+}
+
+// One CTA per (sequence, 4 q heads), one thread per (head, head_dim element).
+// The chunks' (max, sum) pairs and scale factors go through shared memory, so
+// the partial outputs are read with independent loads.
+template <int D>
+__global__ void __launch_bounds__(D * kCombineHeads) decode_combine_kernel(DecodeArgs a) {
+    __shared__ float f_all[kCombineHeads][kCombineChunks];
+    __shared__ float red_all[kCombineHeads][D / 32];
+    __shared__ float M_all[kCombineHeads], L_all[kCombineHeads];
     wait_for_predecessor();                  // the split kernel's partials
-    const int32_t h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const int32_t h = blockIdx.x * kCombineHeads + threadIdx.y, b = blockIdx.y, d = threadIdx.x;
+    if (h >= a.Hq) return;                   // whole head slice: no barrier below is shared
+    float* f = f_all[threadIdx.y];
+    float* red = red_all[threadIdx.y];
+    float& M_s = M_all[threadIdx.y];
+    float& L_s = L_all[threadIdx.y];
     const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
     if (n == 1) return;                                  // written by the split kernel
     const int64_t qh = (int64_t)b * a.Hq + h;
@@ -375,13 +388,13 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (lane == 0) red[w] = M;
-    __syncthreads();
+    slice_sync<D>();
     if (d == 0) {
         float m = red[0];
         for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
         M_s = m;
     }
-    __syncthreads();
+    slice_sync<D>();
     M = M_s;
     float L = 0.f, O = 0.f;
     for (int c0 = 0; c0 < n; c0 += kCombineChunks) {
@@ -395,21 +408,21 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
-        __syncthreads();
+        slice_sync<D>();
         if (lane == 0) red[w] = lpart;
-        __syncthreads();
+        slice_sync<D>();
         if (d == 0) {
             float sum = 0.f;
             for (int i = 0; i < D / 32; ++i) sum += red[i];
             L_s = sum;
         }
-        __syncthreads();
+        slice_sync<D>();
         L += L_s;
         const float* po = a.part_o + ((int64_t)(p0 + c0) * a.Hq + h) * D + d;
         const int64_t step = (int64_t)a.Hq * D;
 #pragma unroll 8
         for (int c = 0; c < cn; ++c) O += f[c] * po[c * step];
-        __syncthreads();
+        slice_sync<D>();
     }
     a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
@@ -497,8 +510,9 @@ int launch_decode(DecodeArgs& a, cudaStream_t s) {
         const int32_t rows = a.B - b0 < 65535 ? a.B - b0 : 65535;
         sub.chunk_prefix = a.chunk_prefix + b0;
         sub.out = a.out + (int64_t)b0 * a.Hq * D;
-        if (launch_dependent(decode_combine_kernel<D>, dim3((unsigned)a.Hq, (unsigned)rows),
-                             dim3(D), s, sub) != cudaSuccess)
+        const unsigned hblocks = (unsigned)((a.Hq + kCombineHeads - 1) / kCombineHeads);
+        if (launch_dependent(decode_combine_kernel<D>, dim3(hblocks, (unsigned)rows),
+                             dim3(D, kCombineHeads), s, sub) != cudaSuccess)
             return PKV_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

@@ -113,7 +113,10 @@ PKV_API int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_ca
 
 /*
  * Bytes of device workspace pkv_paged_decode needs for these sizes (a pure
- * host function; the same arguments give the same answer).
+ * host function; the same arguments give the same answer).  The split into
+ * key chunks depends on the batch, so the size is not monotone in it: a
+ * workspace shared by several batch sizes (e.g. one CUDA graph per size)
+ * must be as large as the largest of their answers.
  */
 PKV_API size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                         int32_t max_context_len, pkv_cache_desc cache);
@@ -175,6 +178,32 @@ PKV_API int pkv_paged_decode_static_workspace(
     int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
     int32_t num_q_heads, int32_t max_context_len, float scale, void* out,
     pkv_cache_desc cache, uint32_t* status, void* stream);
+
+/*
+ * kv_store then paged_decode, enqueued as one call: the per-layer pair the
+ * engine runs every decode step ([LIFE] §2.2.4: store_kvcache, then the
+ * attention op; [UML] §2.4).  Arguments are those of pkv_kv_store (k, v,
+ * slot_mapping, num_tokens) followed by those of pkv_paged_decode; k_cache
+ * and v_cache are written by the store and read by the decode.  The decode's
+ * set-up kernel is launched as a programmatic dependent of the store, so the
+ * two overlap their launch latency; the attention still reads the stored rows.
+ * Arguments are all checked before anything is enqueued.
+ */
+PKV_API int pkv_kv_store_paged_decode(
+    const void* k, const void* v, const int32_t* slot_mapping, int32_t num_tokens,
+    const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+    int32_t num_q_heads, int32_t max_context_len, float scale, void* out, void* workspace,
+    size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status, void* stream);
+
+/*
+ * One layer's k_cache / v_cache inside the whole KV pool the engine allocates
+ * once, [2, num_layers, num_blocks, block_size, num_kv_heads, head_dim] bf16
+ * ([LIFE] §2.2.3: kv_cache[0, l] and kv_cache[1, l] are views, not copies).
+ * Pure host pointer arithmetic; nothing is read or enqueued.
+ */
+PKV_API int pkv_layer_cache(const void* kv_pool, int32_t num_layers, int32_t layer,
+                            pkv_cache_desc cache, const void** k_cache, const void** v_cache);
 
 /*
  * Bytes of device workspace pkv_paged_prefill_varlen needs (pure host function).

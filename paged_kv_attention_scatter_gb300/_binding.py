@@ -32,7 +32,8 @@ STATUS = {v: k for k, v in PKV_STATUS_BITS.items()}
 C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_store",
                "pkv_paged_decode_workspace_bytes", "pkv_paged_decode",
                "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample",
-               "pkv_paged_decode_static_workspace"]
+               "pkv_paged_decode_static_workspace", "pkv_kv_store_paged_decode",
+               "pkv_layer_cache"]
 
 # Size of the scratch array compiled into the library for
 # pkv_paged_decode_static_workspace (PKV_STATIC_DECODE_WORKSPACE_BYTES).
@@ -80,6 +81,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                              I32, F32, P, P, SZ, CacheDesc, P, P]
     lib.pkv_sample.restype = ctypes.c_int
     lib.pkv_sample.argtypes = [P, P, P, I32, I32, P, P, P]
+    lib.pkv_kv_store_paged_decode.restype = ctypes.c_int
+    lib.pkv_kv_store_paged_decode.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, I32,
+                                              F32, P, P, SZ, CacheDesc, P, P]
+    lib.pkv_layer_cache.restype = ctypes.c_int
+    lib.pkv_layer_cache.argtypes = [P, I32, I32, CacheDesc, ctypes.POINTER(ctypes.c_void_p),
+                                    ctypes.POINTER(ctypes.c_void_p)]
     _LIB = lib
     return lib
 
@@ -271,3 +278,48 @@ def paged_decode_static_workspace(q, k_cache, v_cache, block_tables, context_len
             _ptr_or_null(status, "status", torch.int32, dev), _stream(dev, stream))
     _check(rc, "pkv_paged_decode_static_workspace")
     return out
+
+
+def kv_store_paged_decode(k, v, slot_mapping, q, k_cache, v_cache, block_tables, context_lens,
+                          scale, max_context_len, out=None, workspace=None, status=None,
+                          stream=None) -> torch.Tensor:
+    """kv_store of the new tokens followed by paged_decode, in one call."""
+    lib = load()
+    dev = k_cache.device
+    B, Hq, D = q.shape
+    n = slot_mapping.numel()
+    if k.shape != (n,) + tuple(k_cache.shape[2:]) or v.shape != k.shape:
+        raise ValueError("k/v must be [num_tokens, num_kv_heads, head_dim] matching the cache")
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_decode_workspace_bytes(B, Hq, max_context_len, k_cache)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.pkv_kv_store_paged_decode(
+        _dev(k, "k", torch.bfloat16, dev), _dev(v, "v", torch.bfloat16, dev),
+        _dev(slot_mapping, "slot_mapping", torch.int32, dev), n,
+        _dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", torch.bfloat16, dev),
+        _dev(v_cache, "v_cache", torch.bfloat16, dev),
+        _dev(block_tables, "block_tables", torch.int32, dev), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32, dev), B, Hq, int(max_context_len),
+        float(scale), _dev(out, "out", torch.bfloat16, dev),
+        _dev(workspace, "workspace", torch.uint8, dev), workspace.numel(), cache_desc(k_cache),
+        _ptr_or_null(status, "status", torch.int32, dev), _stream(dev, stream))
+    _check(rc, "pkv_kv_store_paged_decode")
+    return out
+
+
+def layer_cache(kv_pool: torch.Tensor, layer: int):
+    """(k_cache, v_cache) views of one layer of a [2, L, NB, bs, Hkv, D] bf16 pool.
+    The layer's addresses come from pkv_layer_cache (checked against the views)."""
+    if kv_pool.dim() != 6 or kv_pool.shape[0] != 2 or not kv_pool.is_contiguous():
+        raise ValueError("kv_pool must be a contiguous [2, L, NB, bs, Hkv, D] tensor")
+    L, nb, bs, hkv, d = kv_pool.shape[1:]
+    kp, vp = ctypes.c_void_p(), ctypes.c_void_p()
+    rc = load().pkv_layer_cache(kv_pool.data_ptr(), L, int(layer), CacheDesc(nb, bs, hkv, d),
+                                ctypes.byref(kp), ctypes.byref(vp))
+    _check(rc, "pkv_layer_cache")
+    kc, vc = kv_pool[0, layer], kv_pool[1, layer]
+    if kc.data_ptr() != kp.value or vc.data_ptr() != vp.value:
+        raise RuntimeError("pkv_layer_cache disagrees with the tensor layout")
+    return kc, vc

@@ -43,3 +43,18 @@ extern "C" const char* pkv_status_string(uint32_t bits) {
     if (bits & PKV_STATUS_WAIT_TIMEOUT) return "a bounded in-kernel wait gave up";
     return "unknown status bit";
 }
+
+extern "C" int pkv_layer_cache(const void* kv_pool, int32_t num_layers, int32_t layer,
+                               pkv_cache_desc cache, const void** k_cache,
+                               const void** v_cache) {
+    if (!kv_pool || !k_cache || !v_cache) return PKV_ERR_NULL_POINTER;
+    if (num_layers <= 0 || layer < 0 || layer >= num_layers || cache.num_blocks <= 0 ||
+        cache.block_size <= 0 || cache.num_kv_heads <= 0 || cache.head_dim <= 0)
+        return PKV_ERR_BAD_DIMENSION;
+    const size_t layer_bytes = (size_t)cache.num_blocks * cache.block_size *
+                               cache.num_kv_heads * cache.head_dim * 2;
+    const char* base = (const char*)kv_pool;
+    *k_cache = base + (size_t)layer * layer_bytes;
+    *v_cache = base + ((size_t)num_layers + layer) * layer_bytes;
+    return PKV_OK;
+}

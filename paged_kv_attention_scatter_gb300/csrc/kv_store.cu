@@ -22,6 +22,9 @@ __global__ void __launch_bounds__(256) kv_store_kernel(
         uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
         const int32_t* __restrict__ slot_mapping, int32_t num_tokens,
         int32_t row_vecs, int64_t num_slots, uint32_t* status) {
+    // a decode launched after this store may start its set-up now; it waits
+    // for this grid's stores before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t total = (int64_t)num_tokens * row_vecs;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;

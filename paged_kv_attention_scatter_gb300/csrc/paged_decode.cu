@@ -123,6 +123,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
         __syncthreads();
     }
     if (threadIdx.x == 0) a.chunk_prefix[0] = 0;
+    // When launched right after a kv_store (pkv_kv_store_paged_decode), finish
+    // only after the store has: the split kernel waits for this grid, so it
+    // then also sees the stored rows.  A no-op for an ordinary launch.
+    wait_for_predecessor();
 }
 
 template <int D>
@@ -495,8 +499,13 @@ int max_resident(const void* fn) {
 }
 
 template <int D>
-int launch_decode(DecodeArgs& a, cudaStream_t s) {
-    decode_plan_kernel<<<1, 1024, 0, s>>>(a);
+int launch_decode(DecodeArgs& a, cudaStream_t s, bool after_store = false) {
+    if (after_store) {
+        if (launch_dependent(decode_plan_kernel, dim3(1), dim3(1024), s, a) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    } else {
+        decode_plan_kernel<<<1, 1024, 0, s>>>(a);
+    }
     const int per_sm = max_resident<D>((const void*)decode_split_kernel<D>);
     const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;
     int64_t grid = (int64_t)pkv_num_sms() * per_sm;
@@ -529,18 +538,20 @@ extern "C" size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_
     return decode_layout(batch, num_q_heads, max_context_len, cache).total;
 }
 
-extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* v_cache,
-                                const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                const int32_t* context_lens, int32_t batch,
-                                int32_t num_q_heads, int32_t max_context_len, float scale,
-                                void* out, void* workspace, size_t workspace_bytes,
-                                pkv_cache_desc cache, uint32_t* status, void* stream) {
+namespace {
+
+// Checks the arguments and fills `a`; PKV_OK means the decode may be launched.
+int make_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                     int32_t max_context_len, float scale, void* out, void* workspace,
+                     size_t workspace_bytes, const pkv_cache_desc& cache, uint32_t* status,
+                     DecodeArgs& a) {
     if (batch < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 ||
         cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0)
         return PKV_ERR_BAD_DIMENSION;
     if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_BAD_DIMENSION;
     if (cache.head_dim != 64 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED_HEAD_DIM;
-    if (batch == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return PKV_ERR_NULL_POINTER;
     if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out |
@@ -550,7 +561,6 @@ extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* 
     const DecodeLayout L = decode_layout(batch, num_q_heads, max_context_len, cache);
     if (workspace_bytes < L.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
     char* ws = (char*)workspace;
-    DecodeArgs a;
     a.q = (const __nv_bfloat16*)q;
     a.kc = (const __nv_bfloat16*)k_cache;
     a.vc = (const __nv_bfloat16*)v_cache;
@@ -573,8 +583,47 @@ extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* 
     a.cap = L.cap;
     a.scale_log2 = scale * pkv::kLog2e;
     a.status = status;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t batch,
+                                int32_t num_q_heads, int32_t max_context_len, float scale,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                pkv_cache_desc cache, uint32_t* status, void* stream) {
+    if (batch == 0 && max_context_len >= 0 && num_q_heads > 0) return PKV_OK;
+    DecodeArgs a;
+    const int rc = make_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    context_lens, batch, num_q_heads, max_context_len, scale, out,
+                                    workspace, workspace_bytes, cache, status, a);
+    if (rc != PKV_OK) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     return cache.head_dim == 128 ? launch_decode<128>(a, s) : launch_decode<64>(a, s);
+}
+
+extern "C" int pkv_kv_store_paged_decode(
+        const void* k, const void* v, const int32_t* slot_mapping, int32_t num_tokens,
+        const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
+        int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+        int32_t num_q_heads, int32_t max_context_len, float scale, void* out, void* workspace,
+        size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status, void* stream) {
+    if (batch == 0 && max_context_len >= 0 && num_q_heads > 0)
+        return pkv_kv_store(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache, status,
+                            stream);
+    DecodeArgs a;
+    int rc = make_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                              context_lens, batch, num_q_heads, max_context_len, scale, out,
+                              workspace, workspace_bytes, cache, status, a);
+    if (rc != PKV_OK) return rc;                 // nothing enqueued
+    rc = pkv_kv_store(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache, status, stream);
+    if (rc != PKV_OK) return rc;                 // nothing enqueued
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool chained = num_tokens > 0;         // an empty store launches nothing
+    return cache.head_dim == 128 ? launch_decode<128>(a, s, chained)
+                                 : launch_decode<64>(a, s, chained);
 }
 
 // ---------------------------------------------------------------------------

@@ -72,3 +72,18 @@ def test_host_checks_return_codes_without_a_gpu(lib):
     # a misaligned pointer is rejected on the host; it is never dereferenced
     p = ctypes.c_void_p(16 * 1024 + 2)
     assert lib.pkv_sample(p, p, p, 1, 10, p, None, None) == -4
+
+
+def test_layer_cache_pointer_arithmetic(lib):
+    """[LIFE] §2.2.3: the pool is [2, L, NB, bs, Hkv, D]; layer l's K is
+    kv_cache[0, l] and its V kv_cache[1, l] (views).  Host arithmetic only."""
+    from paged_kv_attention_scatter_gb300._binding import CacheDesc
+    c = CacheDesc(10, 16, 2, 64)
+    layer_bytes = 10 * 16 * 2 * 64 * 2
+    base = 1 << 20
+    kp, vp = ctypes.c_void_p(), ctypes.c_void_p()
+    assert lib.pkv_layer_cache(base, 4, 3, c, ctypes.byref(kp), ctypes.byref(vp)) == 0
+    assert kp.value == base + 3 * layer_bytes
+    assert vp.value == base + (4 + 3) * layer_bytes
+    assert lib.pkv_layer_cache(base, 4, 4, c, ctypes.byref(kp), ctypes.byref(vp)) == -2
+    assert lib.pkv_layer_cache(None, 4, 0, c, ctypes.byref(kp), ctypes.byref(vp)) == -1

@@ -306,9 +306,17 @@ def bench_sample(pkv, W, torch, dev, pk):
         gm.replay()
     t = time_graph(gm, 50, torch)
     b = 8.0 * spec.batch * spec.vocab + 8 * spec.batch
+    gp = graph_of(lambda: pkv.sample_philox(lg, tp, 1234, 0, out=ids), torch)
+    for _ in range(3):
+        gp.replay()
+    tpx = time_graph(gp, 50, torch)
+    bp = 4.0 * spec.batch * spec.vocab + 8 * spec.batch
     return {"sample": {"workload": f"B={spec.batch} V={spec.vocab}", "us": round(t * 1e6, 2),
                        "gbs": round(b / t / 1e9, 1), "frac_hbm": round(b / t / 1e9 / pk["hbm"], 4),
-                       "bytes": b, "timing": "CUDA graph replays (inputs 622 MB > L2)"}}
+                       "bytes": b, "timing": "CUDA graph replays (inputs 622 MB > L2)"},
+            "sample_philox": {"workload": f"B={spec.batch} V={spec.vocab}, noise drawn in kernel",
+                              "us": round(tpx * 1e6, 2), "gbs": round(bp / tpx / 1e9, 1),
+                              "frac_hbm": round(bp / tpx / 1e9 / pk["hbm"], 4), "bytes": bp}}
 
 
 def bench_kvstore(pkv, W, torch, dev, pk, flush):

@@ -267,6 +267,20 @@ PKV_API int pkv_sample(const float* logits, const float* temperatures, const flo
                int32_t batch, int32_t vocab, int32_t* out_token_ids,
                uint32_t* status, void* stream);
 
+/*
+ * sample with the Exp(1) noise drawn inside the kernel instead of read from
+ * memory (halves the sampler's HBM bytes).  The noise of entry n = row*vocab+i
+ * comes from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
+ * numbers: as easy as 1, 2, 3", SC 2011) with key = seed (low word first) and
+ * counter = (n/4 low, n/4 high, offset low, offset high), output word n%4:
+ * U = ((w >> 8) + 1) * 2^-24 in (0, 1], E = -ln U.  Everything else is as in
+ * pkv_sample (temperature, lowest-index ties, status bits).  The same (seed,
+ * offset) gives the same draw; advance `offset` per step for fresh noise.
+ */
+PKV_API int pkv_sample_philox(const float* logits, const float* temperatures, uint64_t seed,
+                              uint64_t offset, int32_t batch, int32_t vocab,
+                              int32_t* out_token_ids, uint32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

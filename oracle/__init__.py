@@ -40,6 +40,12 @@ Functions and their pins (all pins are tests under ``tests/`` marked not-gpu):
       P(token k) = softmax(logits/T)_k by a chi-square test, and to the
       lowest-index tie rule.
 
-No function here is "parity unpinned".
+  sampler.philox4x32_10 / philox_words / philox_exp_noise / sample_philox
+      the counter-based noise of the in-kernel-noise sampler.  Parity
+      unpinned for the generator itself (no published known-answer vector is
+      used); checked by inverting its round, by output statistics, and by the
+      Gumbel-max law of the draws it feeds.
+
+Every other function is pinned.
 """
 from . import attention, kv_store, sampler, slots  # noqa: F401

@@ -14,6 +14,14 @@ Readings where the pages are silent (listed in the design doc):
   * ties go to the lowest index;
   * a temperature that is not a positive finite number is a precondition
     violation: the row returns token 0 and is reported.
+
+In-kernel noise (the library's second sampler entry point) uses the
+counter-based generator Philox4x32-10 of Salmon, Moraes, Dror and Shaw,
+"Parallel random numbers: as easy as 1, 2, 3" (SC 2011), restated below from
+that definition.  `philox4x32_10` is "parity unpinned": no published
+known-answer vector is used; it is checked only by statistics of its output,
+by inverting its round function, and through the Gumbel-max law of the draws
+it feeds.
 """
 from __future__ import annotations
 
@@ -77,3 +85,66 @@ def near_ties(keys: np.ndarray, rel: float = 1e-5):
         tol = rel * max(1.0, abs(top)) if np.isfinite(top) else 0.0
         out.append(np.flatnonzero(row >= top - tol))
     return out
+
+
+# ----------------------------------------------------------------------------
+# counter-based Exp(1) noise
+# ----------------------------------------------------------------------------
+PHILOX_M = (0xD2511F53, 0xCD9E8D57)       # round multipliers
+PHILOX_W = (0x9E3779B9, 0xBB67AE85)       # key schedule increments (Weyl sequence)
+MASK32 = 0xFFFFFFFF
+
+
+def philox_round(c, k0, k1):
+    """One Philox4x32 round on counters c (N, 4) of 32-bit values held in
+    uint64: multiply words 0 and 2 by the two constants, split each 64-bit
+    product into (hi, lo), and output (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0)."""
+    p0 = np.uint64(PHILOX_M[0]) * c[:, 0]
+    p1 = np.uint64(PHILOX_M[1]) * c[:, 2]
+    hi0, lo0 = p0 >> np.uint64(32), p0 & np.uint64(MASK32)
+    hi1, lo1 = p1 >> np.uint64(32), p1 & np.uint64(MASK32)
+    return np.stack([hi1 ^ c[:, 1] ^ np.uint64(k0), lo1, hi0 ^ c[:, 3] ^ np.uint64(k1), lo0],
+                    axis=1)
+
+
+def philox4x32_10(counters, key):
+    """Ten rounds; the 64-bit key (k0, k1) is bumped by the Weyl increments
+    before every round after the first.  counters: (N, 4) integers < 2^32.
+    Returns (N, 4) uint64 words < 2^32."""
+    c = np.asarray(counters, dtype=np.uint64)
+    k0, k1 = int(key[0]) & MASK32, int(key[1]) & MASK32
+    for r in range(10):
+        if r > 0:
+            k0 = (k0 + PHILOX_W[0]) & MASK32
+            k1 = (k1 + PHILOX_W[1]) & MASK32
+        c = philox_round(c, k0, k1)
+    return c
+
+
+def philox_words(n, seed: int, offset: int):
+    """Output word of entry n (a flat index): Philox4x32-10 keyed by the 64-bit
+    seed on counter (n // 4 as two 32-bit words, offset as two 32-bit words),
+    word n % 4."""
+    n = np.asarray(n, dtype=np.uint64).reshape(-1)
+    blk = n >> np.uint64(2)
+    ctr = np.stack([blk & np.uint64(MASK32), blk >> np.uint64(32),
+                    np.full_like(blk, offset & MASK32), np.full_like(blk, (offset >> 32) & MASK32)],
+                   axis=1)
+    w = philox4x32_10(ctr, (seed & MASK32, (seed >> 32) & MASK32))
+    return w[np.arange(len(n)), (n & np.uint64(3)).astype(np.int64)]
+
+
+def philox_exp_noise(batch: int, vocab: int, seed: int, offset: int):
+    """(B, V) Exp(1) noise: entry n = row * vocab + i draws word w, U = (w >> 8
+    plus one) * 2^-24 (exact, in (0, 1]) and E = -ln U (float64)."""
+    n = np.arange(batch * vocab, dtype=np.uint64)
+    w = philox_words(n, seed, offset)
+    u = ((w >> np.uint64(8)) + np.uint64(1)).astype(np.float64) * 2.0 ** -24
+    return (-np.log(u)).reshape(batch, vocab)
+
+
+def sample_philox(logits, temperatures, seed: int, offset: int):
+    """The draw of `sample` with the noise of `philox_exp_noise`."""
+    lg = np.asarray(logits)
+    E = philox_exp_noise(lg.shape[0], lg.shape[1], seed, offset)
+    return sample(lg, temperatures, E)

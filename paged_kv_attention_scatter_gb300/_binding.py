@@ -33,7 +33,7 @@ C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_s
                "pkv_paged_decode_workspace_bytes", "pkv_paged_decode",
                "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample",
                "pkv_paged_decode_static_workspace", "pkv_kv_store_paged_decode",
-               "pkv_layer_cache"]
+               "pkv_layer_cache", "pkv_sample_philox"]
 
 # Size of the scratch array compiled into the library for
 # pkv_paged_decode_static_workspace (PKV_STATIC_DECODE_WORKSPACE_BYTES).
@@ -84,6 +84,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pkv_kv_store_paged_decode.restype = ctypes.c_int
     lib.pkv_kv_store_paged_decode.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, I32,
                                               F32, P, P, SZ, CacheDesc, P, P]
+    lib.pkv_sample_philox.restype = ctypes.c_int
+    lib.pkv_sample_philox.argtypes = [P, P, ctypes.c_uint64, ctypes.c_uint64, I32, I32, P, P, P]
     lib.pkv_layer_cache.restype = ctypes.c_int
     lib.pkv_layer_cache.argtypes = [P, I32, I32, CacheDesc, ctypes.POINTER(ctypes.c_void_p),
                                     ctypes.POINTER(ctypes.c_void_p)]
@@ -323,3 +325,24 @@ def layer_cache(kv_pool: torch.Tensor, layer: int):
     if kc.data_ptr() != kp.value or vc.data_ptr() != vp.value:
         raise RuntimeError("pkv_layer_cache disagrees with the tensor layout")
     return kc, vc
+
+
+def sample_philox(logits, temperatures, seed: int, offset: int, out=None, status=None,
+                  stream=None) -> torch.Tensor:
+    """Gumbel-max sampling with in-kernel Philox4x32-10 Exp(1) noise: logits
+    [B, V] fp32, temperatures [B] fp32 -> token ids [B] int32."""
+    lib = load()
+    dev = logits.device
+    B, V = logits.shape
+    if temperatures.shape != (B,):
+        raise ValueError("temperatures must be [batch]")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = lib.pkv_sample_philox(_dev(logits, "logits", torch.float32, dev),
+                               _dev(temperatures, "temperatures", torch.float32, dev),
+                               int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), B, V,
+                               _dev(out, "out", torch.int32, dev),
+                               _ptr_or_null(status, "status", torch.int32, dev),
+                               _stream(dev, stream))
+    _check(rc, "pkv_sample_philox")
+    return out

@@ -16,6 +16,13 @@
 // lowest index at every level, so the result does not depend on the split.
 // No workspace and no second launch: the cluster barrier is a hardware
 // barrier of co-scheduled CTAs, not a spin on memory.
+//
+// A second entry point draws the noise in the kernel instead of reading it:
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011) keyed by a 64-bit seed, with counter
+// (n / 4 as 64 bits, offset as 64 bits) for entry n = row * vocab + i, word
+// n % 4 of the four outputs; U = (word / 2^8 + 1) / 2^24 in (0, 1] and
+// E = -ln U.  The row then costs 4 bytes per entry instead of 8.
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
@@ -44,10 +51,46 @@ __device__ __forceinline__ float gumbel_key(float logit, float inv_t, float e) {
     return logit * inv_t - __logf(fmaxf(e, kNoiseFloor));
 }
 
+// ---- Philox4x32-10 (the published round function and key schedule) ----
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += kPhiloxW0;
+            k1 += kPhiloxW1;
+        }
+        const uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
+        const uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// Exp(1) noise from one Philox output word: U = (w / 2^8 + 1) / 2^24, E = -ln U.
+// logf (not the fast log): U close to 1 gives a tiny E that needs relative accuracy.
+__device__ __forceinline__ float exp_noise_of(uint32_t w) {
+    const float u = (float)((w >> 8) + 1u) * 5.9604644775390625e-8f;   // 2^-24
+    return -logf(u);
+}
+
+__device__ __forceinline__ uint4 philox_block(uint64_t n4, uint64_t seed, uint64_t offset) {
+    return philox4x32_10(make_uint4((uint32_t)n4, (uint32_t)(n4 >> 32), (uint32_t)offset,
+                                    (uint32_t)(offset >> 32)),
+                         (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& w, int j) {
+    return j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+}
+
+template <bool kPhilox>
 __global__ void __launch_bounds__(kThreads) sample_kernel(
         const float* __restrict__ logits, const float* __restrict__ temperatures,
-        const float* __restrict__ noise, int32_t row0, int32_t vocab, bool vec_ok,
-        int32_t* __restrict__ out, uint32_t* status) {
+        const float* __restrict__ noise, uint64_t seed, uint64_t offset, int32_t row0,
+        int32_t vocab, bool vec_ok, int32_t* __restrict__ out, uint32_t* status) {
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int csize = (int)cluster.num_blocks();
@@ -63,29 +106,47 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
     if (t_ok) {
         const float inv_t = 1.0f / temp;
         const float* lrow = logits + row * vocab;
-        const float* nrow = noise + row * vocab;
+        const float* nrow = kPhilox ? nullptr : noise + row * vocab;
         // contiguous segment of this CTA, a multiple of 4 entries long
         int seg = (vocab + csize - 1) / csize;
         seg = (seg + 3) & ~3;
         const int lo = min(vocab, rank * seg);
         const int hi = min(vocab, lo + seg);
+        const uint64_t n_row = (uint64_t)row * (uint64_t)vocab;
         if (vec_ok) {
-            // rows start 16-byte aligned: lo is a multiple of 4
+            // rows start 16-byte aligned: lo is a multiple of 4 (and so is n_row)
             const int nvec = (hi - lo) >> 2;
             for (int v = threadIdx.x; v < nvec; v += kThreads) {
                 const int i = lo + 4 * v;
                 const float4 l4 = pkv::ld_stream16f(lrow + i);
-                const float4 e4 = pkv::ld_stream16f(nrow + i);
+                float4 e4;
+                if (kPhilox) {
+                    const uint4 w = philox_block((n_row + i) >> 2, seed, offset);
+                    e4 = make_float4(exp_noise_of(w.x), exp_noise_of(w.y), exp_noise_of(w.z),
+                                     exp_noise_of(w.w));
+                } else {
+                    e4 = pkv::ld_stream16f(nrow + i);
+                }
                 take_if_better(best, gumbel_key(l4.x, inv_t, e4.x), i);
                 take_if_better(best, gumbel_key(l4.y, inv_t, e4.y), i + 1);
                 take_if_better(best, gumbel_key(l4.z, inv_t, e4.z), i + 2);
                 take_if_better(best, gumbel_key(l4.w, inv_t, e4.w), i + 3);
             }
-            for (int i = lo + 4 * nvec + threadIdx.x; i < hi; i += kThreads)
-                take_if_better(best, gumbel_key(lrow[i], inv_t, nrow[i]), i);
+            for (int i = lo + 4 * nvec + threadIdx.x; i < hi; i += kThreads) {
+                const float e = kPhilox ? exp_noise_of(word_of(
+                                              philox_block((n_row + i) >> 2, seed, offset),
+                                              (int)((n_row + i) & 3)))
+                                        : nrow[i];
+                take_if_better(best, gumbel_key(lrow[i], inv_t, e), i);
+            }
         } else {
-            for (int i = lo + threadIdx.x; i < hi; i += kThreads)
-                take_if_better(best, gumbel_key(lrow[i], inv_t, nrow[i]), i);
+            for (int i = lo + threadIdx.x; i < hi; i += kThreads) {
+                const float e = kPhilox ? exp_noise_of(word_of(
+                                              philox_block((n_row + i) >> 2, seed, offset),
+                                              (int)((n_row + i) & 3)))
+                                        : nrow[i];
+                take_if_better(best, gumbel_key(lrow[i], inv_t, e), i);
+            }
         }
     }
     // warp, then CTA
@@ -126,18 +187,12 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
     cluster.sync();                       // keep shared memory alive for rank 0
 }
 
-}  // namespace
-
-extern "C" int pkv_sample(const float* logits, const float* temperatures,
-                          const float* exp_noise, int32_t batch, int32_t vocab,
-                          int32_t* out_token_ids, uint32_t* status, void* stream) {
-    if (batch < 0 || vocab <= 0) return PKV_ERR_BAD_DIMENSION;
-    if (batch == 0) return PKV_OK;
-    if (!logits || !temperatures || !exp_noise || !out_token_ids) return PKV_ERR_NULL_POINTER;
-    if (((uintptr_t)logits | (uintptr_t)temperatures | (uintptr_t)exp_noise |
-         (uintptr_t)out_token_ids) & 3)
-        return PKV_ERR_MISALIGNED;
-    const bool vec_ok = (vocab % 4 == 0) && ((((uintptr_t)logits) | ((uintptr_t)exp_noise)) & 15) == 0;
+template <bool kPhilox>
+int launch_sample(const float* logits, const float* temperatures, const float* exp_noise,
+                  uint64_t seed, uint64_t offset, int32_t batch, int32_t vocab,
+                  int32_t* out_token_ids, uint32_t* status, void* stream) {
+    const bool vec_ok = (vocab % 4 == 0) &&
+                        ((((uintptr_t)logits) | ((uintptr_t)exp_noise)) & 15) == 0;
     int csize = (vocab + 16383) / 16384;           // about 16K entries per CTA
     if (csize > 8) csize = 8;
     if (csize < 1) csize = 1;
@@ -155,9 +210,37 @@ extern "C" int pkv_sample(const float* logits, const float* temperatures,
         cfg.stream = (cudaStream_t)stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel, logits, temperatures, exp_noise,
-                                           r0, vocab, vec_ok, out_token_ids, status);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel<kPhilox>, logits, temperatures,
+                                           exp_noise, seed, offset, r0, vocab, vec_ok,
+                                           out_token_ids, status);
         if (e != cudaSuccess) return PKV_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int pkv_sample(const float* logits, const float* temperatures,
+                          const float* exp_noise, int32_t batch, int32_t vocab,
+                          int32_t* out_token_ids, uint32_t* status, void* stream) {
+    if (batch < 0 || vocab <= 0) return PKV_ERR_BAD_DIMENSION;
+    if (batch == 0) return PKV_OK;
+    if (!logits || !temperatures || !exp_noise || !out_token_ids) return PKV_ERR_NULL_POINTER;
+    if (((uintptr_t)logits | (uintptr_t)temperatures | (uintptr_t)exp_noise |
+         (uintptr_t)out_token_ids) & 3)
+        return PKV_ERR_MISALIGNED;
+    return launch_sample<false>(logits, temperatures, exp_noise, 0, 0, batch, vocab,
+                                out_token_ids, status, stream);
+}
+
+extern "C" int pkv_sample_philox(const float* logits, const float* temperatures,
+                                 uint64_t seed, uint64_t offset, int32_t batch, int32_t vocab,
+                                 int32_t* out_token_ids, uint32_t* status, void* stream) {
+    if (batch < 0 || vocab <= 0) return PKV_ERR_BAD_DIMENSION;
+    if (batch == 0) return PKV_OK;
+    if (!logits || !temperatures || !out_token_ids) return PKV_ERR_NULL_POINTER;
+    if (((uintptr_t)logits | (uintptr_t)temperatures | (uintptr_t)out_token_ids) & 3)
+        return PKV_ERR_MISALIGNED;
+    return launch_sample<true>(logits, temperatures, nullptr, seed, offset, batch, vocab,
+                               out_token_ids, status, stream);
 }

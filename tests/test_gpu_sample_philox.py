@@ -1,0 +1,63 @@
+"""The in-kernel-noise sampler against the oracle's restatement of the same
+Philox4x32-10 stream."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as U
+from oracle import sampler as osm
+from paged_kv_attention_scatter_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("vocab", [4096, 4099])
+@pytest.mark.parametrize("seed,offset", [(0, 0), (12345, 3), ((1 << 40) + 7, (1 << 33) + 1)])
+def test_equal_logits_pick_the_largest_word_exactly(cuda, vocab, seed, offset):
+    """With equal logits the key is -ln E = -ln(-ln U): the token is the entry
+    with the largest U, i.e. the largest word >> 8, an integer decision the
+    oracle makes exactly from its own Philox stream."""
+    pkv = U.lib()
+    B = 16
+    ids = pkv.sample_philox(torch.zeros((B, vocab), device=cuda),
+                            torch.ones(B, device=cuda), seed, offset).cpu().numpy()
+    w = osm.philox_words(np.arange(B * vocab), seed, offset).reshape(B, vocab) >> np.uint64(8)
+    assert np.array_equal(ids, np.argmax(w, axis=1))
+
+
+def test_spiked_logits_full_vocab_rows(cuda):
+    pkv = U.lib()
+    g = torch.Generator().manual_seed(4)
+    logits, temps, _ = W.sampler_inputs(12, 151936, 3.0, 4, 0.2, 1.2, g)
+    ids = pkv.sample_philox(logits.to(cuda), temps.to(cuda), 99, 5).cpu().numpy()
+    ref, bad = osm.sample_philox(logits.numpy(), temps.numpy(), 99, 5)
+    E = osm.philox_exp_noise(12, 151936, 99, 5)
+    _, keys = osm.sample_key_form(logits.numpy(), temps.numpy(), E)
+    near = osm.near_ties(keys)
+    assert not bad
+    for r in range(12):
+        assert ids[r] == ref[r] or (len(near[r]) > 1 and ids[r] in near[r])
+
+
+def test_draws_follow_the_gumbel_law(cuda):
+    from scipy.stats import chisquare
+    pkv = U.lib()
+    row = torch.tensor([1.0, -0.5, 2.0, 0.0, 0.3, -2.0, 1.2, 0.8])
+    draws = 40_000
+    ids = pkv.sample_philox(row.repeat(draws, 1).to(cuda), torch.full((draws,), 0.8, device=cuda),
+                            2024, 0).cpu().numpy()
+    counts = np.bincount(ids, minlength=8)
+    x = row.double().numpy() / 0.8
+    p = np.exp(x - x.max())
+    p /= p.sum()
+    assert chisquare(counts, p * draws).pvalue > 1e-4
+
+
+def test_bad_temperature_rows(cuda):
+    pkv = U.lib()
+    st = pkv.new_status(cuda)
+    ids = pkv.sample_philox(torch.randn(3, 100, device=cuda),
+                            torch.tensor([1.0, 0.0, float("inf")], device=cuda), 1, 1,
+                            status=st).cpu().tolist()
+    assert ids[1:] == [0, 0]
+    assert U.status_word(st) == pkv.STATUS["BAD_TEMPERATURE"]

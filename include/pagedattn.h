@@ -249,6 +249,26 @@ PKV_API int pkv_paged_prefill_varlen(const void* q, const void* k, const void* v
                              pkv_cache_desc cache, uint32_t* status, void* stream);
 
 /*
+ * kv_store followed by paged_prefill_varlen on the same stream: the per-layer
+ * pair of a prefill round, cache write then attention ([LIFE] §2.2.4 and §4
+ * store_kvcache before the attention op; [UML] §2.4).  The store writes this
+ * call's k/v rows (total_q of them) to slot_mapping's slots (negative =
+ * padding, skipped); the other arguments are those of
+ * pkv_paged_prefill_varlen, with k_cache/v_cache written by the store and
+ * required even when block_tables is NULL.  The prefill's tile plan is launched
+ * as a programmatic dependent of the store, and the attention reads nothing
+ * until both are done.  Every argument is checked before anything is
+ * enqueued.
+ */
+PKV_API int pkv_kv_store_paged_prefill_varlen(
+    const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+    const int32_t* slot_mapping, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+    int32_t batch, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+    int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq, float scale,
+    void* out, void* workspace, size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status,
+    void* stream);
+
+/*
  * sample -- temperature, softmax and Gumbel-max sampling of one token per row
  * ([UML] §2.4: "温度、softmax和gumbel max"; [LIFE] §4: the sampler runs on each
  * sequence's last-position logits).  With supplied Exp(1) noise E the draw is

@@ -33,6 +33,7 @@ C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_s
                "pkv_paged_decode_workspace_bytes", "pkv_paged_decode",
                "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample",
                "pkv_paged_decode_static_workspace", "pkv_kv_store_paged_decode",
+               "pkv_kv_store_paged_prefill_varlen",
                "pkv_layer_cache", "pkv_sample_philox"]
 
 # Size of the scratch array compiled into the library for
@@ -84,6 +85,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pkv_kv_store_paged_decode.restype = ctypes.c_int
     lib.pkv_kv_store_paged_decode.argtypes = [P, P, P, I32, P, P, P, P, I32, P, I32, I32, I32,
                                               F32, P, P, SZ, CacheDesc, P, P]
+    lib.pkv_kv_store_paged_prefill_varlen.restype = ctypes.c_int
+    lib.pkv_kv_store_paged_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32,
+                                                      I32, I32, P, I32, F32, P, P, SZ,
+                                                      CacheDesc, P, P]
     lib.pkv_sample_philox.restype = ctypes.c_int
     lib.pkv_sample_philox.argtypes = [P, P, ctypes.c_uint64, ctypes.c_uint64, I32, I32, P, P, P]
     lib.pkv_layer_cache.restype = ctypes.c_int
@@ -229,6 +234,40 @@ def paged_prefill_varlen(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, 
         workspace.numel(), desc, _ptr_or_null(status, "status", torch.int32, dev),
         _stream(dev, stream))
     _check(rc, "pkv_paged_prefill_varlen")
+    return out
+
+
+def kv_store_paged_prefill_varlen(q, k, v, k_cache, v_cache, slot_mapping, cu_seqlens_q,
+                                  cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_tables, scale,
+                                  out=None, workspace=None, status=None,
+                                  stream=None) -> torch.Tensor:
+    """kv_store of the chunk's k/v rows (slot_mapping [Tq] int32) followed by
+    paged_prefill_varlen, in one call.  block_tables may be None when no
+    sequence has a cached prefix; the cache is always written."""
+    lib = load()
+    dev = q.device
+    T, Hq, D = q.shape
+    B = cu_seqlens_q.numel() - 1
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must hold one slot per query token")
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_prefill_workspace_bytes(B, T, Hq, tuple(k_cache.shape))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.pkv_kv_store_paged_prefill_varlen(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k, "k", torch.bfloat16, dev),
+        _dev(v, "v", torch.bfloat16, dev), _dev(k_cache, "k_cache", torch.bfloat16, dev),
+        _dev(v_cache, "v_cache", torch.bfloat16, dev),
+        _dev(slot_mapping, "slot_mapping", torch.int32, dev),
+        _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev),
+        _dev(cu_seqlens_k, "cu_seqlens_k", torch.int32, dev), B, T, int(max_seqlen_q),
+        int(max_seqlen_k), Hq, _ptr_or_null(block_tables, "block_tables", torch.int32, dev),
+        block_tables.shape[1] if block_tables is not None else 0, float(scale),
+        _dev(out, "out", torch.bfloat16, dev), _dev(workspace, "workspace", torch.uint8, dev),
+        workspace.numel(), cache_desc(k_cache), _ptr_or_null(status, "status", torch.int32, dev),
+        _stream(dev, stream))
+    _check(rc, "pkv_kv_store_paged_prefill_varlen")
     return out
 
 

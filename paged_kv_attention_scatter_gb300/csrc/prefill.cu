@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
         a.sched[0] = min(total, a.max_tiles);
         a.sched[1] = 0;
     }
+    // Launched after a store, the plan completes only once the store's writes
+    // are visible, so the attention kernels' wait on the plan covers both.
+    // Without a programmatic predecessor this returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsG) prefill_general_kernel(PrefillArgs 
 }
 
 template <int D>
-int launch_general(PrefillArgs& a, cudaStream_t s) {
+int launch_general(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre) {
     const size_t smem = (size_t)(kBM + 4 * kBN) * (D / 8) * 16;
     static bool configured = false;
     if (!configured) {
@@ -360,6 +364,10 @@ int launch_general(PrefillArgs& a, cudaStream_t s) {
             return PKV_ERR_CUDA;
         configured = true;
     }
+    a.tile_m = kBM;
+    a.tile_n = kBN;
+    const int rc = pkv_launch_prefill_plan(a, s, pre);
+    if (rc != PKV_OK) return rc;
     for (int32_t base = 0; base < a.max_tiles; base += 65535) {
         const int32_t n = a.max_tiles - base < 65535 ? a.max_tiles - base : 65535;
         cudaLaunchAttribute attr[1];
@@ -390,31 +398,44 @@ PrefillLayout pkv_prefill_layout(int32_t batch, int32_t total_q) {
     return L;
 }
 
-int pkv_launch_prefill_plan(PrefillArgs& a, cudaStream_t s) {
-    prefill_plan_kernel<<<1, 1024, 0, s>>>(a);
+int pkv_launch_prefill_plan(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre) {
+    bool chained = false;
+    if (pre) {
+        const int rc = pre->enqueue(pre->ctx, &chained);
+        if (rc != PKV_OK) return rc;
+    }
+    if (!chained) {
+        prefill_plan_kernel<<<1, 1024, 0, s>>>(a);
+    } else {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, 1);
+        cfg.blockDim = dim3(1024, 1, 1);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, prefill_plan_kernel, a) != cudaSuccess) return PKV_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // tcgen05 fast path (prefill_tc.cu): returns PKV_ERR_UNSUPPORTED when the
 // shapes are not its own.
 int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim);
-int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s);
+int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre);
 
-extern "C" size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,
-                                                    int32_t num_q_heads, pkv_cache_desc cache) {
-    (void)num_q_heads;
-    (void)cache;
-    if (batch < 0 || total_q < 0) return 0;
-    return pkv_prefill_layout(batch, total_q).total;
-}
+namespace {
 
-extern "C" int pkv_paged_prefill_varlen(
-        const void* q, const void* k, const void* v, const void* k_cache, const void* v_cache,
-        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
-        int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
-        const int32_t* block_tables, int32_t max_blocks_per_seq, float scale, void* out,
-        void* workspace, size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status,
-        void* stream) {
+// Checks every argument and fills the kernel arguments; enqueues nothing.
+int make_prefill_args(const void* q, const void* k, const void* v, const void* k_cache,
+                      const void* v_cache, const int32_t* cu_seqlens_q,
+                      const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+                      int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
+                      const int32_t* block_tables, int32_t max_blocks_per_seq, float scale,
+                      void* out, void* workspace, size_t workspace_bytes, pkv_cache_desc cache,
+                      uint32_t* status, PrefillArgs& a) {
     if (batch < 0 || total_q < 0 || num_q_heads <= 0 || cache.num_kv_heads <= 0 ||
         max_seqlen_q < 0 || max_seqlen_k < 0)
         return PKV_ERR_BAD_DIMENSION;
@@ -436,7 +457,6 @@ extern "C" int pkv_paged_prefill_varlen(
     const PrefillLayout L = pkv_prefill_layout(batch, total_q);
     if (workspace_bytes < L.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
     char* ws = (char*)workspace;
-    PrefillArgs a;
     a.q = (const __nv_bfloat16*)q;
     a.k = (const __nv_bfloat16*)k;
     a.v = (const __nv_bfloat16*)v;
@@ -461,11 +481,78 @@ extern "C" int pkv_paged_prefill_varlen(
     a.max_tiles = L.max_tiles;
     a.scale_log2 = scale * pkv::kLog2e;
     a.status = status;
-    cudaStream_t s = (cudaStream_t)stream;
-    if (pkv_prefill_tc_supported(a, cache.head_dim) == PKV_OK) return pkv_launch_prefill_tc(a, s);
-    a.tile_m = kBM;
-    a.tile_n = kBN;
-    int rc = pkv_launch_prefill_plan(a, s);
-    if (rc != PKV_OK) return rc;
-    return cache.head_dim == 128 ? launch_general<128>(a, s) : launch_general<64>(a, s);
+    return PKV_OK;
+}
+
+int launch_prefill(PrefillArgs& a, int head_dim, cudaStream_t s, const PrefillPrologue* pre) {
+    if (pkv_prefill_tc_supported(a, head_dim) == PKV_OK) return pkv_launch_prefill_tc(a, s, pre);
+    return head_dim == 128 ? launch_general<128>(a, s, pre) : launch_general<64>(a, s, pre);
+}
+
+// The chunk's kv_store, run as the prologue of a fused prefill.
+struct StoreCall {
+    const void* k;
+    const void* v;
+    void* k_cache;
+    void* v_cache;
+    const int32_t* slot_mapping;
+    int32_t num_tokens;
+    pkv_cache_desc cache;
+    uint32_t* status;
+    void* stream;
+};
+
+int enqueue_store(void* ctx, bool* launched) {
+    const StoreCall& c = *(const StoreCall*)ctx;
+    *launched = c.num_tokens > 0;                 // an empty store launches nothing
+    return pkv_kv_store(c.k, c.v, c.k_cache, c.v_cache, c.slot_mapping, c.num_tokens, c.cache,
+                        c.status, c.stream);
+}
+
+}  // namespace
+
+extern "C" size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,
+                                                    int32_t num_q_heads, pkv_cache_desc cache) {
+    (void)num_q_heads;
+    (void)cache;
+    if (batch < 0 || total_q < 0) return 0;
+    return pkv_prefill_layout(batch, total_q).total;
+}
+
+extern "C" int pkv_paged_prefill_varlen(
+        const void* q, const void* k, const void* v, const void* k_cache, const void* v_cache,
+        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+        int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
+        const int32_t* block_tables, int32_t max_blocks_per_seq, float scale, void* out,
+        void* workspace, size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status,
+        void* stream) {
+    PrefillArgs a;
+    const int rc = make_prefill_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                                     batch, total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
+                                     block_tables, max_blocks_per_seq, scale, out, workspace,
+                                     workspace_bytes, cache, status, a);
+    if (rc != PKV_OK || batch == 0 || total_q == 0) return rc;
+    return launch_prefill(a, cache.head_dim, (cudaStream_t)stream, nullptr);
+}
+
+extern "C" int pkv_kv_store_paged_prefill_varlen(
+        const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+        const int32_t* slot_mapping, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+        int32_t batch, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+        int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+        float scale, void* out, void* workspace, size_t workspace_bytes, pkv_cache_desc cache,
+        uint32_t* status, void* stream) {
+    PrefillArgs a;
+    const int rc = make_prefill_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                                     batch, total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
+                                     block_tables, max_blocks_per_seq, scale, out, workspace,
+                                     workspace_bytes, cache, status, a);
+    if (rc != PKV_OK) return rc;                              // nothing enqueued
+    StoreCall store{k, v, k_cache, v_cache, slot_mapping, total_q, cache, status, stream};
+    if (batch == 0 || total_q == 0) {
+        bool launched = false;
+        return enqueue_store(&store, &launched);
+    }
+    const PrefillPrologue pre{enqueue_store, &store};
+    return launch_prefill(a, cache.head_dim, (cudaStream_t)stream, &pre);
 }

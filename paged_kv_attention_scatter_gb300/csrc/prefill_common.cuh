@@ -44,4 +44,16 @@ struct PrefillLayout {
 };
 
 PrefillLayout pkv_prefill_layout(int32_t batch, int32_t total_q);
-int pkv_launch_prefill_plan(pkv::PrefillArgs& a, cudaStream_t s);
+
+// Work a fused entry point enqueues ahead of the prefill on the same stream
+// (the chunk's kv_store).  The launchers run it after every host-side step
+// that can fail, so a rejected call enqueues nothing.  When it launched a
+// grid, the tile plan is launched as that grid's programmatic dependent and
+// finishes only after it (the attention kernels wait for the plan).
+struct PrefillPrologue {
+    int (*enqueue)(void* ctx, bool* launched);
+    void* ctx;
+};
+
+// Enqueues `pre` (may be null), then the tile plan.
+int pkv_launch_prefill_plan(pkv::PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre);

@@ -439,7 +439,7 @@ int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
     return PKV_OK;
 }
 
-int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s) {
+int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre) {
     TcMaps maps;
     if (!encode_rows(&maps.q, a.q, a.total_q, a.Hq) ||
         !encode_rows(&maps.k, a.k, a.total_q, a.Hkv) ||
@@ -453,10 +453,6 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s) {
         maps.kc = maps.k;
         maps.vc = maps.v;
     }
-    a.tile_m = kBM;
-    a.tile_n = kBN;
-    int rc = pkv_launch_prefill_plan(a, s);
-    if (rc != PKV_OK) return rc;
     const int smem = (int)sizeof(TcSmem) + 1024;
     static bool configured = false;
     if (!configured) {
@@ -465,6 +461,10 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s) {
             return PKV_ERR_CUDA;
         configured = true;
     }
+    a.tile_m = kBM;
+    a.tile_n = kBN;
+    const int rc = pkv_launch_prefill_plan(a, s, pre);
+    if (rc != PKV_OK) return rc;
     int64_t grid = pkv_num_sms();
     const int64_t upper = (int64_t)a.max_tiles * a.Hq;
     if (grid > upper) grid = upper;

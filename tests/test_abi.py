@@ -69,9 +69,18 @@ def test_host_checks_return_codes_without_a_gpu(lib):
                                 CacheDesc(8, 4, 2, 64), None, None) == -2
     assert lib.pkv_paged_prefill_varlen(None, None, None, None, None, None, None, 1, 4, 4, 4,
                                         2, None, 0, 1.0, None, None, 0, c, None, None) == -1
+    # the fused store + prefill checks the prefill's arguments before enqueueing the store
+    assert lib.pkv_kv_store_paged_prefill_varlen(None, None, None, None, None, None, None, None,
+                                                 1, 4, 4, 4, 2, None, 0, 1.0, None, None, 0, c,
+                                                 None, None) == -1
+    assert lib.pkv_kv_store_paged_prefill_varlen(None, None, None, None, None, None, None, None,
+                                                 1, 4, 4, 4, 2, None, 0, 0.0, None, None, 0, c,
+                                                 None, None) == -2
     # a misaligned pointer is rejected on the host; it is never dereferenced
     p = ctypes.c_void_p(16 * 1024 + 2)
     assert lib.pkv_sample(p, p, p, 1, 10, p, None, None) == -4
+    assert lib.pkv_kv_store_paged_prefill_varlen(p, p, p, p, p, p, p, p, 1, 4, 4, 4, 2, None, 0,
+                                                 1.0, p, p, 1 << 20, c, None, None) == -4
 
 
 def test_layer_cache_pointer_arithmetic(lib):

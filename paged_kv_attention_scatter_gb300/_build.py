@@ -18,7 +18,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpagedattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "kv_store.cu", "paged_decode.cu", "prefill.cu", "prefill_tc.cu",
+SOURCES = ["api.cu", "kv_store.cu", "paged_decode.cu", "paged_decode_tma.cu", "prefill.cu",
+           "prefill_tc.cu",
            "sample.cu"]
 
 

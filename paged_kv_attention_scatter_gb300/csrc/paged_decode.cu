@@ -38,45 +38,20 @@
 //    stalls the K/V stream.)
 //  * Keys past ctx_b are never loaded (their registers are zero and their
 //    scores -inf), so NaN in unused cache slots cannot reach the output.
-#include "common.cuh"
+#include "decode_common.cuh"
 
 namespace {
+
+using pkv::DecodeArgs;
+using pkv::kMaxGroup;
+using pkv::allow_dependent_launch;
+using pkv::pair;
+using pkv::wait_for_predecessor;
+using pkv::word;
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStep = 16;            // keys per warp step
-constexpr int kMaxGroup = 8;         // q heads per unit (mma rows 0..7)
-
-struct DecodeArgs {
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* kc;
-    const __nv_bfloat16* vc;
-    const int32_t* bt;
-    const int32_t* ctx;
-    __nv_bfloat16* out;
-    int32_t* chunk_prefix;           // [B+1] exclusive prefix of chunk counts
-    float2* part_ml;                 // [cap * Hq]: (max, sum) in base 2
-    float* part_o;                   // [cap * Hq * D]
-    int32_t B, Hq, Hkv, G, n_hg, MB, NB, bs, max_ctx, chunk_keys, cap;
-    float scale_log2;
-    uint32_t* status;
-};
-
-__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-// pack (lo = element e of a, hi = element e of b), e in 0..7 of a 16-byte chunk
-__device__ __forceinline__ uint32_t pair(const uint4& a, const uint4& b, int e) {
-    return __byte_perm(word(a, e >> 1), word(b, e >> 1), (e & 1) ? 0x7632 : 0x5410);
-}
-
-__device__ __forceinline__ void allow_dependent_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void wait_for_predecessor() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
     allow_dependent_launch();
@@ -117,7 +92,14 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
         }
         __syncthreads();
         const int32_t incl = x + (w > 0 ? warp_sums[w - 1] : 0) + carry;
-        if (b < a.B) a.chunk_prefix[b + 1] = incl;
+        if (b < a.B) {
+            a.chunk_prefix[b + 1] = incl;
+            // one record per chunk: what the split kernels need to start it
+            const int32_t c = n > 0 ? a.ctx[b] : 0;
+            for (int32_t i = 0; i < n; ++i)
+                a.chunk_info[incl - n + i] =
+                    make_int4(b, i * a.chunk_keys, min(c, (i + 1) * a.chunk_keys), n);
+        }
         __syncthreads();
         if (threadIdx.x == blockDim.x - 1) carry = incl;
         __syncthreads();
@@ -463,7 +445,7 @@ int32_t choose_chunk_keys(int32_t batch, int32_t units_per_seq_chunk, int32_t ma
 
 struct DecodeLayout {
     int32_t chunk_keys, cap;
-    size_t off_prefix, off_ml, off_o, total;
+    size_t off_prefix, off_info, off_ml, off_o, total;
 };
 
 DecodeLayout decode_layout(int32_t batch, int32_t num_q_heads, int32_t max_ctx,
@@ -476,7 +458,8 @@ DecodeLayout decode_layout(int32_t batch, int32_t num_q_heads, int32_t max_ctx,
     L.cap = (int32_t)((int64_t)batch * per_seq);
     auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
     L.off_prefix = 0;
-    L.off_ml = align(L.off_prefix + sizeof(int32_t) * ((size_t)batch + 1));
+    L.off_info = align(L.off_prefix + sizeof(int32_t) * ((size_t)batch + 1));
+    L.off_ml = align(L.off_info + sizeof(int4) * (size_t)L.cap);
     L.off_o = align(L.off_ml + sizeof(float2) * (size_t)L.cap * num_q_heads);
     L.total = align(L.off_o + sizeof(float) * (size_t)L.cap * num_q_heads * c.head_dim);
     return L;
@@ -506,14 +489,19 @@ int launch_decode(DecodeArgs& a, cudaStream_t s, bool after_store = false) {
     } else {
         decode_plan_kernel<<<1, 1024, 0, s>>>(a);
     }
-    const int per_sm = max_resident<D>((const void*)decode_split_kernel<D>);
-    const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;
-    int64_t grid = (int64_t)pkv_num_sms() * per_sm;
-    if (grid > upper) grid = upper;
-    if (grid < 1) grid = 1;
-    if (launch_dependent(decode_split_kernel<D>, dim3((unsigned)grid), dim3(kThreads), s, a) !=
-        cudaSuccess)
-        return PKV_ERR_CUDA;
+    if (pkv_decode_tma_supported(a, D) == PKV_OK) {
+        const int rc = pkv_launch_decode_tma(a, D, s);
+        if (rc != PKV_OK) return rc;
+    } else {
+        const int per_sm = max_resident<D>((const void*)decode_split_kernel<D>);
+        const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;
+        int64_t grid = (int64_t)pkv_num_sms() * per_sm;
+        if (grid > upper) grid = upper;
+        if (grid < 1) grid = 1;
+        if (launch_dependent(decode_split_kernel<D>, dim3((unsigned)grid), dim3(kThreads), s,
+                             a) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
     for (int32_t b0 = 0; b0 < a.B; b0 += 65535) {
         DecodeArgs sub = a;
         const int32_t rows = a.B - b0 < 65535 ? a.B - b0 : 65535;
@@ -568,6 +556,7 @@ int make_decode_args(const void* q, const void* k_cache, const void* v_cache,
     a.ctx = context_lens;
     a.out = (__nv_bfloat16*)out;
     a.chunk_prefix = (int32_t*)(ws + L.off_prefix);
+    a.chunk_info = (int4*)(ws + L.off_info);
     a.part_ml = (float2*)(ws + L.off_ml);
     a.part_o = (float*)(ws + L.off_o);
     a.B = batch;

@@ -43,6 +43,7 @@
 
 #include "prefill_common.cuh"
 #include "tc_utils.cuh"
+#include "tma_host.cuh"
 
 using pkv::PrefillArgs;
 using namespace pkv::tc;
@@ -399,34 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-    }
-    return fn;
-}
-
-// [rows, heads, 128] bf16 viewed as a 3-D tensor (head_dim innermost); box =
-// 64 elements (128 B, the swizzle width) x 1 head x 128 rows.
+// [rows, heads, 128] bf16, box 64 x 1 head x 128 rows.
 bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
-    cuuint32_t box[3] = {64, 1, 128};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return pkv::tma_encode_rows(m, base, rows, heads, kD, 128);
 }
 
 }  // namespace
@@ -435,7 +411,7 @@ int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
     if (head_dim != kD) return PKV_ERR_UNSUPPORTED;
     if (a.bt != nullptr && (a.bs % kBN) != 0) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)a.NB * a.bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
-    if (encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
+    if (pkv::tma_encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
 }
 

@@ -84,8 +84,11 @@ def test_step_8b_store_then_decode_sampled(cuda):
     U.assert_close(U.f64(out)[seqs], ref[seqs], "step-8b decode")
 
 
+# block sizes that are multiples of 64 run the TMA-fed split kernel, the others
+# the register-load one; 16 q heads per kv head make two head groups per unit
 @pytest.mark.parametrize("hq,hkv,d,bs", [(4, 4, 128, 16), (16, 1, 128, 256), (8, 2, 64, 4),
-                                         (6, 2, 64, 32), (12, 4, 128, 64)])
+                                         (6, 2, 64, 32), (12, 4, 128, 64), (16, 1, 64, 64),
+                                         (8, 8, 64, 128), (32, 2, 128, 128)])
 def test_shapes_and_block_sizes(cuda, hq, hkv, d, bs):
     pkv = U.lib()
     spec = W.DecodeSpec(f"shape {hq}/{hkv}x{d} bs{bs}", seed=hq * 31 + bs, batch=7,
@@ -95,10 +98,11 @@ def test_shapes_and_block_sizes(cuda, hq, hkv, d, bs):
     _decode(pkv, w, cuda)
 
 
-def test_zero_and_one_key_contexts(cuda):
+@pytest.mark.parametrize("bs", [16, 64])
+def test_zero_and_one_key_contexts(cuda, bs):
     pkv = U.lib()
     spec = W.DecodeSpec("edge", seed=9, batch=5, num_q_heads=8, num_kv_heads=2, head_dim=128,
-                        block_size=16, ctx_lo=1, ctx_hi=40)
+                        block_size=bs, ctx_lo=1, ctx_hi=40)
     w = W.decode_workload(spec)
     w.context_lens[0] = 0
     w.context_lens[1] = 1
@@ -120,10 +124,11 @@ def test_context_over_stated_maximum_is_reported(cuda):
     assert over and float(out[over].abs().max()) == 0.0
 
 
-def test_bad_block_id_is_reported_not_read(cuda):
+@pytest.mark.parametrize("bs", [16, 64])
+def test_bad_block_id_is_reported_not_read(cuda, bs):
     pkv = U.lib()
     spec = W.DecodeSpec("badblk", seed=12, batch=3, num_q_heads=4, num_kv_heads=1,
-                        head_dim=128, block_size=16, ctx_lo=40, ctx_hi=60)
+                        head_dim=128, block_size=bs, ctx_lo=2 * bs + 8, ctx_hi=4 * bs - 4)
     w = W.decode_workload(spec)
     w.block_tables[1, 1] = 10_000_000
     st = pkv.new_status(cuda)

@@ -335,80 +335,51 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     }
 }
 
-constexpr int kCombineChunks = 256;  // chunks whose factors are staged at once
-
+constexpr int kCombineBatch = 8;     // chunks whose partials are loaded at once
 constexpr int kCombineHeads = 4;     // q heads per combine CTA
 
-// Barrier of the D threads of one head slice (threadIdx.y) of a combine CTA.
-template <int D>
-__device__ __forceinline__ void slice_sync() {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + (int)threadIdx.y), "n"(D) : "memory");
-}
-
 // One CTA per (sequence, 4 q heads), one thread per (head, head_dim element).
-// The chunks' (max, sum) pairs and scale factors go through shared memory, so
-// the partial outputs are read with independent loads.
+// Each thread merges the chunks' partials of its element online, loading the
+// (max, sum) pairs and the partial outputs of up to 8 chunks at once, so the
+// whole merge is one round trip per 8 chunks with no block-wide reduction.
 template <int D>
-__global__ void __launch_bounds__(D * kCombineHeads) decode_combine_kernel(DecodeArgs a) {
-    __shared__ float f_all[kCombineHeads][kCombineChunks];
-    __shared__ float red_all[kCombineHeads][D / 32];
-    __shared__ float M_all[kCombineHeads], L_all[kCombineHeads];
+__global__ void __launch_bounds__(D * kCombineHeads, 2) decode_combine_kernel(DecodeArgs a) {
     wait_for_predecessor();                  // the split kernel's partials
     const int32_t h = blockIdx.x * kCombineHeads + threadIdx.y, b = blockIdx.y, d = threadIdx.x;
-    if (h >= a.Hq) return;                   // whole head slice: no barrier below is shared
-    float* f = f_all[threadIdx.y];
-    float* red = red_all[threadIdx.y];
-    float& M_s = M_all[threadIdx.y];
-    float& L_s = L_all[threadIdx.y];
+    if (h >= a.Hq) return;
     const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
     if (n == 1) return;                                  // written by the split kernel
     const int64_t qh = (int64_t)b * a.Hq + h;
-    if (n == 0) {                                        // empty or rejected sequence
-        a.out[qh * D + d] = __float2bfloat16_rn(0.f);
-        return;
-    }
-    const int lane = d & 31, w = d >> 5;
-    // block max of the chunks' maxima
-    float M = -INFINITY;
-    for (int c = d; c < n; c += D) M = fmaxf(M, a.part_ml[(int64_t)(p0 + c) * a.Hq + h].x);
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    for (int32_t c0 = 0; c0 < n; c0 += kCombineBatch) {
+        const int cn = min(kCombineBatch, n - c0);
+        float2 ml[kCombineBatch];
+        float ov[kCombineBatch];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) red[w] = M;
-    slice_sync<D>();
-    if (d == 0) {
-        float m = red[0];
-        for (int i = 1; i < D / 32; ++i) m = fmaxf(m, red[i]);
-        M_s = m;
-    }
-    slice_sync<D>();
-    M = M_s;
-    float L = 0.f, O = 0.f;
-    for (int c0 = 0; c0 < n; c0 += kCombineChunks) {
-        const int cn = min(kCombineChunks, n - c0);
-        float lpart = 0.f;
-        for (int c = d; c < cn; c += D) {
-            const float2 ml = a.part_ml[(int64_t)(p0 + c0 + c) * a.Hq + h];
-            const float fc = (ml.x == -INFINITY) ? 0.f : pkv::fast_exp2(ml.x - M);
-            f[c] = fc;
-            lpart += ml.y * fc;
+        for (int c = 0; c < kCombineBatch; ++c) {
+            ml[c] = make_float2(-INFINITY, 0.f);
+            ov[c] = 0.f;
+            if (c < cn) {
+                const int64_t slot = (int64_t)(p0 + c0 + c) * a.Hq + h;
+                ml[c] = a.part_ml[slot];
+                ov[c] = a.part_o[slot * D + d];
+            }
         }
+        float mb = M;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
-        slice_sync<D>();
-        if (lane == 0) red[w] = lpart;
-        slice_sync<D>();
-        if (d == 0) {
-            float sum = 0.f;
-            for (int i = 0; i < D / 32; ++i) sum += red[i];
-            L_s = sum;
+        for (int c = 0; c < kCombineBatch; ++c) mb = fmaxf(mb, ml[c].x);
+        if (mb == -INFINITY) continue;                   // nothing visible yet
+        const float r = (M == -INFINITY) ? 0.f : pkv::fast_exp2(M - mb);
+        L *= r;
+        O *= r;
+#pragma unroll
+        for (int c = 0; c < kCombineBatch; ++c) {
+            if (ml[c].x == -INFINITY) continue;
+            const float f = pkv::fast_exp2(ml[c].x - mb);
+            L += ml[c].y * f;
+            O += ov[c] * f;
         }
-        slice_sync<D>();
-        L += L_s;
-        const float* po = a.part_o + ((int64_t)(p0 + c0) * a.Hq + h) * D + d;
-        const int64_t step = (int64_t)a.Hq * D;
-#pragma unroll 8
-        for (int c = 0; c < cn; ++c) O += f[c] * po[c * step];
-        slice_sync<D>();
+        M = mb;
     }
     a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }

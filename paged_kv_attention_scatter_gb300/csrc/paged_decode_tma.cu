@@ -57,7 +57,7 @@ struct Cfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kStageBytes = 2 * kHalves * kTileBytes;    // K halves, then V halves
     static constexpr int kQBytes = kMaxGroup * D * 2;
-    static constexpr int kStages = D == 128 ? 6 : 10;
+    static constexpr int kStages = D == 128 ? 5 : 10;   // 5 x 32 KB measured faster than 6
 };
 
 template <int D>

@@ -32,6 +32,26 @@ METRIC = "paged decode HBM GB/s (% of peak) & prefill tokens/s (% TC peak), 1 GB
 L2_BYTES = 129e6
 LAYERS_0P6B = 28                   # decoder layers of a Qwen3-0.6B-shaped model
 
+# DRAM bytes (read + write) of one decode-0.6b paged_decode call, summed over
+# its plan, split and combine launches, from one ncu capture (profiles/
+# decode_tma_kernel_decode-0.6b.md).  Valid only for the decode sources it was
+# taken on: the digest below must match, otherwise the traffic is reported null.
+DECODE_0P6B_TRAFFIC = {"bytes": 585880064,
+                       "sources_sha256": "41bb9ae96534c7e89bff247f03d4b1c0268897c3957fdc8e09ba90c256ff0d4e"}
+DECODE_SOURCES = ["paged_decode.cu", "paged_decode_tma.cu", "decode_common.cuh", "common.cuh",
+                  "tc_utils.cuh", "tma_host.cuh"]
+
+
+def decode_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "paged_kv_attention_scatter_gb300", "csrc")
+    for f in DECODE_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -299,7 +319,10 @@ def run_ours(args, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": round(nbytes / step_s / 1e9, 2),
                      "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(nbytes / step_s / 1e9 / pk["hbm"], 4),
-                     "traffic": None, "peak_source": pk["source"],
+                     "traffic": (DECODE_0P6B_TRAFFIC["bytes"]
+                                 if decode_sources_digest() ==
+                                 DECODE_0P6B_TRAFFIC["sources_sha256"] else None),
+                     "traffic_unit": "bytes per call", "peak_source": pk["source"],
                      "kernel": "paged_decode call (plan + split-KV + combine launches), "
                                "28 per step",
                      "bytes_per_launch": nbytes / LAYERS_0P6B},
@@ -567,6 +590,57 @@ def cpu_oracle(steps, warmup, per_step, budget_s):
 
 
 # ----------------------------------------------------------------------------
+def profile_case(name: str, calls: int):
+    """A small case for ncu: `calls` eager calls of one operation on a
+    single-layer workload (inputs above L2, a few GB on the device at most).
+    Prints one line when done; no timing."""
+    import torch
+
+    import paged_kv_attention_scatter_gb300 as pkv
+    from paged_kv_attention_scatter_gb300 import workloads as W
+
+    pkv.build()
+    pkv.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if name == "decode-0.6b":
+        spec = W.DECODE_0P6B
+        w = W.decode_workload(spec, device=dev)
+        bt, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
+        out = torch.empty_like(w.q)
+        ws = torch.empty(pkv.paged_decode_workspace_bytes(spec.batch, spec.num_q_heads,
+                                                          w.max_context_len, w.k_cache),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(calls):
+            pkv.paged_decode(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale, w.max_context_len,
+                             out=out, workspace=ws)
+    elif name == "prefill-8b":
+        spec = W.PREFILL_8B
+        w = W.prefill_workload(spec)
+        st = w.steps[0]
+        kc, vc = w.k_cache0.to(dev), w.v_cache0.to(dev)
+        q, k, v = st.q.to(dev), st.k.to(dev), st.v.to(dev)
+        cu_q, cu_k = st.cu_seqlens_q.to(dev), st.cu_seqlens_k.to(dev)
+        bt, sl = st.block_tables.to(dev), st.slot_mapping.to(dev)
+        for _ in range(calls):
+            pkv.kv_store(k, v, kc, vc, sl)
+            pkv.paged_prefill_varlen(q, k, v, kc, vc, cu_q, cu_k, st.max_seqlen_q,
+                                     st.max_seqlen_k, bt, w.scale)
+    elif name == "sample":
+        spec = W.STEP_8B
+        g = torch.Generator().manual_seed(spec.seed)
+        lg, tp, en = W.sampler_inputs(spec.batch, spec.vocab, spec.logit_sigma,
+                                      spec.logit_spikes, spec.t_lo, spec.t_hi, g)
+        lg, tp, en = lg.to(dev), tp.to(dev), en.to(dev)
+        for _ in range(calls):
+            pkv.sample(lg, tp, en)
+            pkv.sample_philox(lg, tp, 1234, 0)
+    else:
+        raise SystemExit(f"unknown profile case {name!r}")
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": name, "calls": calls}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -581,8 +655,15 @@ def main():
     ap.add_argument("--oracle-worker", action="store_true")
     ap.add_argument("--per-step", type=int, default=1)
     ap.add_argument("--budget", type=float, default=20.0)
+    ap.add_argument("--profile", default=None,
+                    help="run a small case for ncu instead of the benchmark: decode-0.6b, "
+                         "prefill-8b or sample (calls = --steps)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+
+    if args.profile:
+        profile_case(args.profile, args.steps)
+        return
 
     if args.oracle_worker:
         oracle_worker(args.budget, args.steps, args.warmup, args.per_step)

@@ -151,3 +151,25 @@ def test_workspace_too_small_is_rejected(cuda):
         pkv.paged_decode(w.q.to(cuda), w.k_cache.to(cuda), w.v_cache.to(cuda),
                          w.block_tables.to(cuda), w.context_lens.to(cuda), w.scale,
                          w.max_context_len, workspace=ws)
+
+
+@pytest.mark.parametrize("max_ctx_scale", [1, 64])
+def test_stated_maximum_context_sets_the_chunking(cuda, max_ctx_scale):
+    """The chunk size comes from the stated maximum context alone: the exact
+    maximum gives 64-key chunks (up to 15 per sequence), a 64x larger one
+    512-key chunks.  Both chunkings must match the oracle."""
+    pkv = U.lib()
+    spec = W.DecodeSpec("merge", seed=77, batch=24, num_q_heads=8, num_kv_heads=4, head_dim=128,
+                        block_size=64, ctx_lo=1, ctx_hi=900)
+    w = W.decode_workload(spec)
+    max_ctx = int(w.context_lens.max()) * max_ctx_scale
+    bt_cols = -(-max_ctx // spec.block_size)
+    bt = torch.full((spec.batch, bt_cols), -1, dtype=torch.int32)
+    bt[:, :w.block_tables.shape[1]] = w.block_tables
+    st = pkv.new_status(cuda)
+    out = pkv.paged_decode(w.q.to(cuda), w.k_cache.to(cuda), w.v_cache.to(cuda), bt.to(cuda),
+                           w.context_lens.to(cuda), w.scale, max_ctx, status=st)
+    assert U.status_word(st) == 0
+    ref = oatt.paged_decode(U.f64(w.q), w.k_cache, w.v_cache, w.block_tables.numpy(),
+                            w.context_lens.numpy(), w.scale)
+    U.assert_close(U.f64(out), ref, f"decode, max_ctx x{max_ctx_scale}")

@@ -18,7 +18,7 @@
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
 // shared memory because unused cache slots may hold NaN.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (224 threads, one CTA per SM):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks (diagonal and partial tiles only), keeps a running row
 //              maximum that is only raised (and O, l rescaled) when the new
@@ -27,12 +27,18 @@
 //              buffer; at the end it normalises O.
 //   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
 //              three-stage ring.
-//   warp 5     MMA issuer (one thread): S = Q K^T (both operands K-major in
-//              shared memory) into one of three TMEM S buffers, then
-//              O += P V with P read from TMEM and V MN-major in shared memory.
-//              The next tile's Q K^T is issued before waiting for this tile's
-//              P, so the tensor pipe overlaps the softmax; Q K^T into a buffer
-//              waits for the P V that last read P from it.  Also owns TMEM.
+//   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
+//              shared memory) into one of three TMEM S buffers, running up to
+//              two tiles ahead of the softmax; Q K^T into a buffer waits for
+//              the P V that last read P from it.  Also owns TMEM.
+//   warp 6     P V issuer (one thread): O += P V with P read from TMEM and V
+//              MN-major in shared memory, as soon as the softmax has stored P.
+//   Two issuers, because one thread that also waits on four barriers and
+//   commits three times per tile leaves the tensor pipe idle between its
+//   groups of MMAs (a 128x128x16 MMA takes 64 cycles when the pipe is fed);
+//   with two, the waits of one overlap the MMAs of the other.  Descriptors are
+//   built once: a later stage or K slice only adds a constant to the address
+//   field.
 // Keeping P in TMEM means shared memory only carries Q, K and V: an SS MMA of
 // 128x128x16 already reads 128 bytes per clock from it.
 // TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512); stage,
@@ -55,7 +61,7 @@ constexpr int kBN = 128;                 // keys per tile
 constexpr int kD = 128;                  // head_dim
 constexpr int kTile = kBM * kD * 2;      // bytes of one bf16 128x128 tile
 constexpr int kHalf = kTile / 2;         // one 64-column half (128 rows x 128 B)
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             mbar_init(&s.pv_done[i], 1);
         }
         mbar_init(&s.o_free, 128);
-        mbar_init(&s.mma_done, 1);
+        mbar_init(&s.mma_done, 2);
         mbar_init_fence();
     }
     if (warp == 5) tmem_alloc(&s.tmem_base, 512);
@@ -203,63 +209,67 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 }
             }
         }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 5 || warp == 6) {
+        // ------------------------------------------------------------ MMA issuers
+        // warp 5 issues Q K^T, warp 6 issues P V: the barrier waits of one
+        // overlap the MMAs of the other, so the tensor pipe stays fed
         if (lane == 0) {
             const uint32_t id_qk = umma_idesc_bf16(kBM, kBN, false);
             const uint32_t id_pv = umma_idesc_bf16(kBM, kD, true);
-            const uint32_t q_addr = saddr(s.q);
+            const uint64_t qd0 = umma_desc_sw128(saddr(s.q), 16, 1024);
+            const uint64_t kd0 = umma_desc_sw128(saddr(s.k[0]), 16, 1024);
+            const uint64_t vd0 = umma_desc_sw128(saddr(s.v[0]), kHalf, 1024);
             uint32_t T = 0, I = 0;
             bool ok = true;
-            auto issue_qk = [&](uint32_t t) -> bool {
-                const int st = t % kStages;
-                if (!mbar_wait(&s.k_full[st], (t / kStages) & 1, &s.abort_flag)) return false;
-                // the S buffer still holds P of tile t-3 until its P V is done
-                if (t >= kStages &&
-                    !mbar_wait(&s.pv_done[st], (t / kStages - 1) & 1, &s.abort_flag))
-                    return false;
-                tc_fence_after();
-                const uint32_t k_addr = saddr(s.k[st]);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma_bf16(tmem + kColS0 + st * kBN, umma_desc_sw128(q_addr + off, 16, 1024),
-                              umma_desc_sw128(k_addr + off, 16, 1024), id_qk, kk > 0);
-                }
-                umma_commit(&s.s_full[st]);
-                return true;
-            };
             for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
                 const Item x = item_at(a, it);
-                if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag))) break;
-                tc_fence_after();
-                if (!(ok = issue_qk(T))) break;
-                for (int32_t j = 0; j < x.n_tiles; ++j) {
-                    const uint32_t t = T + j;
-                    if (j + 1 < x.n_tiles) {
-                        if (!(ok = issue_qk(t + 1))) break;
-                    } else {
-                        umma_commit(&s.q_free);          // every Q K^T of the item issued
-                    }
-                    const int st = t % kStages;
-                    if (!(ok = mbar_wait(&s.p_full[st], (t / kStages) & 1, &s.abort_flag))) break;
-                    if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1, &s.abort_flag)))
-                        break;
-                    if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
-                    tc_fence_after();
-                    const uint32_t v_addr = saddr(s.v[st]);
+                if (warp == 5) {
+                    if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag))) break;
+                    for (int32_t j = 0; j < x.n_tiles; ++j) {
+                        const uint32_t t = T + j;
+                        const int st = t % kStages;
+                        if (!(ok = mbar_wait(&s.k_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                        // the S buffer still holds P of tile t-3 until its P V is done
+                        if (t >= kStages &&
+                            !(ok = mbar_wait(&s.pv_done[st], (t / kStages - 1) & 1, &s.abort_flag)))
+                            break;
+                        tc_fence_after();
+                        const uint64_t kd = kd0 + (uint64_t)(st * (kTile >> 4));
+                        const uint32_t d_s = tmem + kColS0 + st * kBN;
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        umma_bf16_tmem_a(tmem + kColO, tmem + kColS0 + st * kBN + kk * 8,
-                                         umma_desc_sw128(v_addr + kk * 2048, kHalf, 1024), id_pv,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&s.pv_done[st]);
-                    umma_commit(&s.kv_empty[st]);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                            umma_bf16(d_s, qd0 + off, kd + off, id_qk, kk > 0);
+                        }
+                        umma_commit(&s.s_full[st]);
+                    }
+                    if (!ok) break;
+                    umma_commit(&s.q_free);              // every Q K^T of the item issued
+                } else {
+                    for (int32_t j = 0; j < x.n_tiles; ++j) {
+                        const uint32_t t = T + j;
+                        const int st = t % kStages;
+                        if (!(ok = mbar_wait(&s.p_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                        if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1, &s.abort_flag)))
+                            break;
+                        if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                        tc_fence_after();
+                        const uint64_t vd = vd0 + (uint64_t)(st * (kTile >> 4));
+                        const uint32_t a_p = tmem + kColS0 + st * kBN;
+                        const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            umma_bf16_tmem_a(tmem + kColO, a_p + kk * 8, vd + (kk * 2048 >> 4), id_pv,
+                                             kk > 0 ? 1u : acc0);
+                        umma_commit(&s.pv_done[st]);
+                        umma_commit(&s.kv_empty[st]);
+                    }
+                    if (!ok) break;
                 }
                 T += x.n_tiles;
             }
             if (!ok) give_up(s, a.status);
-            // every MMA this thread issued has finished before TMEM is freed
+            // every MMA of both issuers has finished before TMEM is freed
             umma_commit(&s.mma_done);
             mbar_drain(&s.mma_done, 0);
         }

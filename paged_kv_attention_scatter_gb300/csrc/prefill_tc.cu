@@ -22,11 +22,13 @@
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks (diagonal and partial tiles only), keeps a running row
 //              maximum that is only raised (and O, l rescaled) when the new
-//              maximum exceeds it by more than 2^8, and stores P = exp2(S - m)
+//              maximum exceeds it by more than 2^8 (the row maximum and sum are
+//              taken over independent partial chains), and stores P = exp2(S - m)
 //              as packed bf16 back into the first 64 columns of the same S
 //              buffer; at the end it normalises O.
 //   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
-//              three-stage ring.
+//              three-stage ring.  A K stage is refilled as soon as its Q K^T
+//              is done, a V stage once its P V is done.
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for
@@ -71,7 +73,7 @@ struct __align__(1024) TcSmem {
     unsigned char k[kStages][kTile];
     unsigned char v[kStages][kTile];
     uint64_t q_full, q_free;
-    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
     uint64_t s_full[kStages], p_full[kStages], pv_done[kStages];
     uint64_t o_free, mma_done;
     uint32_t tmem_base;
@@ -128,9 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s.k_full[i], 1);
             mbar_init(&s.v_full[i], 1);
-            mbar_init(&s.kv_empty[i], 1);
+            mbar_init(&s.k_empty[i], 1);
+            mbar_init(&s.v_empty[i], 1);
             mbar_init(&s.s_full[i], 1);
-            mbar_init(&s.p_full[i], 128);
+            mbar_init(&s.p_full[i], 4);
             mbar_init(&s.pv_done[i], 1);
         }
         mbar_init(&s.o_free, 128);
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
                     const int st = T % kStages;
                     const uint32_t use = T / kStages;
-                    if (use > 0 && !(ok = mbar_wait(&s.kv_empty[st], (use - 1) & 1, &s.abort_flag)))
+                    if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_flag)))
                         break;
                     const CUtensorMap* mk;
                     const CUtensorMap* mv;
@@ -193,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     mbar_expect_tx(&s.k_full[st], kTile);
                     for (int hf = 0; hf < 2; ++hf)
                         tma_load_3d(s.k[st] + hf * kHalf, mk, &s.k_full[st], hf * 64, kvh, row);
+                    if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag))) {
+                        mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
+                        break;
+                    }
                     mbar_expect_tx(&s.v_full[st], kTile);
                     for (int hf = 0; hf < 2; ++hf)
                         tma_load_3d(s.v[st] + hf * kHalf, mv, &s.v_full[st], hf * 64, kvh, row);
@@ -242,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                             umma_bf16(d_s, qd0 + off, kd + off, id_qk, kk > 0);
                         }
                         umma_commit(&s.s_full[st]);
+                        umma_commit(&s.k_empty[st]);      // K stage free once Q K^T is done
                     }
                     if (!ok) break;
                     umma_commit(&s.q_free);              // every Q K^T of the item issued
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                             umma_bf16_tmem_a(tmem + kColO, a_p + kk * 8, vd + (kk * 2048 >> 4), id_pv,
                                              kk > 0 ? 1u : acc0);
                         umma_commit(&s.pv_done[st]);
-                        umma_commit(&s.kv_empty[st]);
+                        umma_commit(&s.v_empty[st]);
                     }
                     if (!ok) break;
                 }
@@ -302,17 +310,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     lim = i + 1;
                     masked = true;
                 }
-                float mx = -INFINITY;
+                // eight independent partial maxima: no 128-long dependency chain
+                float mxp[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
                 if (masked) {
 #pragma unroll
                     for (int col = 0; col < kBN; ++col) {
                         sv[col] = col < lim ? sv[col] : -INFINITY;
-                        mx = fmaxf(mx, sv[col]);
+                        mxp[col & 7] = fmaxf(mxp[col & 7], sv[col]);
                     }
                 } else {
 #pragma unroll
-                    for (int col = 0; col < kBN; ++col) mx = fmaxf(mx, sv[col]);
+                    for (int col = 0; col < kBN; ++col) mxp[col & 7] = fmaxf(mxp[col & 7], sv[col]);
                 }
+                float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
                 mx *= a.scale_log2;                         // scale > 0 keeps the order
                 const bool raise = mx > m_run + kRescaleThreshold;
                 float alpha = 1.f;
@@ -339,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     }
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                float lsum = 0.f;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};       // independent partial sums
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float pw[32];                               // packed bf16 pairs
@@ -348,12 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         const int col = half * 64 + 2 * e;
                         const float p0 = pkv::fast_exp2(fmaf(sv[col], a.scale_log2, neg_m));
                         const float p1 = pkv::fast_exp2(fmaf(sv[col + 1], a.scale_log2, neg_m));
-                        lsum += p0 + p1;
+                        ls[e & 3] += p0 + p1;
                         pw[e] = __uint_as_float(pkv::pack_bf16(p0, p1));
                     }
                     tmem_st32(s_col + half * 32, pw);           // P aliases S columns 0..63
                 }
-                l_run += lsum;
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 tmem_wait_st();
                 if (partial_cached) {
                     // masked cached slots may hold NaN: zero their V rows
@@ -369,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
-                mbar_arrive(&s.p_full[st]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.p_full[st]);   // one arrival per softmax warp
             }
             if (!ok) break;
             // ---- epilogue: O / l to global ----

@@ -150,6 +150,37 @@ PKV_API int pkv_paged_decode(const void* q, const void* k_cache, const void* v_c
                      pkv_cache_desc cache, uint32_t* status, void* stream);
 
 /*
+ * paged_decode split into a plan and a run, for a caller that attends many
+ * layers over the same sequences: in a model's decode step every layer has the
+ * same context_lens and block_tables, so the chunk schedule is the same for
+ * all of them.  (No counterpart on the pages: it divides pkv_paged_decode's
+ * work; the result is the same.)
+ *
+ * pkv_paged_decode_plan checks context_lens (a length outside
+ * [0, min(max_context_len, max_blocks_per_seq * block_size)] sets
+ * PKV_STATUS_BAD_CONTEXT_LEN and that sequence attends to nothing) and writes
+ * the chunk schedule into the workspace.  pkv_paged_decode_run then attends with
+ * it: the split-KV and combine kernels only.  A run must get the same
+ * context_lens contents, batch, num_q_heads, max_context_len,
+ * max_blocks_per_seq, cache geometry and workspace as the plan it follows, and
+ * the plan must be enqueued earlier on the same stream (or have completed).  Any
+ * number of runs may follow one plan; a run overwrites the workspace's partial
+ * results, so runs sharing a workspace must not overlap.  Arguments have the
+ * meaning they have in pkv_paged_decode.
+ */
+PKV_API int pkv_paged_decode_plan(const int32_t* context_lens, int32_t batch,
+                                  int32_t num_q_heads, int32_t max_context_len,
+                                  int32_t max_blocks_per_seq, void* workspace,
+                                  size_t workspace_bytes, pkv_cache_desc cache,
+                                  uint32_t* status, void* stream);
+PKV_API int pkv_paged_decode_run(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                 int32_t max_context_len, float scale, void* out, void* workspace,
+                                 size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status,
+                                 void* stream);
+
+/*
  * paged_decode without a caller-provided workspace.  (Not an operation of the
  * pages: it exists for callers that cannot allocate device memory where they
  * call -- e.g. a plugin inside a host engine that owns and budgets all device

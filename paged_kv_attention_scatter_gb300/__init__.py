@@ -13,13 +13,14 @@ PyTorch supplies device memory and streams only.  `workloads` draws the seeded
 synthetic inputs the tests and the benchmark use.
 """
 from ._binding import (STATUS, cache_desc, kv_store, kv_store_paged_decode,  # noqa: F401
-                       kv_store_paged_prefill_varlen, layer_cache, library_path, load, new_status, paged_decode,
+                       kv_store_paged_prefill_varlen, layer_cache, library_path, load,
+                       new_status, paged_decode, paged_decode_plan, paged_decode_run,
                        paged_decode_workspace_bytes, paged_prefill_varlen,
                        paged_prefill_workspace_bytes, sample, sample_philox, status_names)
 from ._build import build  # noqa: F401
 
 __all__ = ["kv_store", "paged_decode", "paged_prefill_varlen", "sample", "build", "load",
            "kv_store_paged_decode", "kv_store_paged_prefill_varlen", "layer_cache",
-           "sample_philox",
+           "paged_decode_plan", "paged_decode_run", "sample_philox",
            "paged_decode_workspace_bytes", "paged_prefill_workspace_bytes", "new_status",
            "status_names", "STATUS", "cache_desc", "library_path"]

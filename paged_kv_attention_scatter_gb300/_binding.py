@@ -33,7 +33,8 @@ C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_s
                "pkv_paged_decode_workspace_bytes", "pkv_paged_decode",
                "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample",
                "pkv_paged_decode_static_workspace", "pkv_kv_store_paged_decode",
-               "pkv_kv_store_paged_prefill_varlen",
+               "pkv_kv_store_paged_prefill_varlen", "pkv_paged_decode_plan",
+               "pkv_paged_decode_run",
                "pkv_layer_cache", "pkv_sample_philox"]
 
 # Size of the scratch array compiled into the library for
@@ -75,6 +76,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pkv_paged_decode.restype = ctypes.c_int
     lib.pkv_paged_decode.argtypes = [P, P, P, P, I32, P, I32, I32, I32, F32, P, P, SZ,
                                      CacheDesc, P, P]
+    lib.pkv_paged_decode_plan.restype = ctypes.c_int
+    lib.pkv_paged_decode_plan.argtypes = [P, I32, I32, I32, I32, P, SZ, CacheDesc, P, P]
+    lib.pkv_paged_decode_run.restype = ctypes.c_int
+    lib.pkv_paged_decode_run.argtypes = [P, P, P, P, I32, P, I32, I32, I32, F32, P, P, SZ,
+                                         CacheDesc, P, P]
     lib.pkv_paged_prefill_workspace_bytes.restype = SZ
     lib.pkv_paged_prefill_workspace_bytes.argtypes = [I32, I32, I32, CacheDesc]
     lib.pkv_paged_prefill_varlen.restype = ctypes.c_int
@@ -194,6 +200,53 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, max_con
                               _ptr_or_null(status, "status", torch.int32, dev),
                               _stream(dev, stream))
     _check(rc, "pkv_paged_decode")
+    return out
+
+
+def paged_decode_plan(context_lens, num_q_heads, max_context_len, max_blocks_per_seq, k_cache,
+                      workspace=None, status=None, stream=None) -> torch.Tensor:
+    """The chunk schedule of a decode batch, written into `workspace` (made
+    here when None), for any number of paged_decode_run calls over layers that
+    share these context lengths.  Returns the workspace."""
+    lib = load()
+    dev = k_cache.device
+    B = context_lens.numel()
+    need = paged_decode_workspace_bytes(B, num_q_heads, max_context_len, k_cache)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.pkv_paged_decode_plan(_dev(context_lens, "context_lens", torch.int32, dev), B,
+                                   int(num_q_heads), int(max_context_len),
+                                   int(max_blocks_per_seq),
+                                   _dev(workspace, "workspace", torch.uint8, dev),
+                                   workspace.numel(), cache_desc(k_cache),
+                                   _ptr_or_null(status, "status", torch.int32, dev),
+                                   _stream(dev, stream))
+    _check(rc, "pkv_paged_decode_plan")
+    return workspace
+
+
+def paged_decode_run(q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                     workspace, out=None, status=None, stream=None) -> torch.Tensor:
+    """paged_decode with the schedule a paged_decode_plan call wrote into
+    `workspace` (same context lengths and sizes)."""
+    lib = load()
+    dev = k_cache.device
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.pkv_paged_decode_run(_dev(q, "q", torch.bfloat16, dev),
+                                  _dev(k_cache, "k_cache", torch.bfloat16, dev),
+                                  _dev(v_cache, "v_cache", torch.bfloat16, dev),
+                                  _dev(block_tables, "block_tables", torch.int32, dev),
+                                  block_tables.shape[1],
+                                  _dev(context_lens, "context_lens", torch.int32, dev), B, Hq,
+                                  int(max_context_len), float(scale),
+                                  _dev(out, "out", torch.bfloat16, dev),
+                                  _dev(workspace, "workspace", torch.uint8, dev),
+                                  workspace.numel(), cache_desc(k_cache),
+                                  _ptr_or_null(status, "status", torch.int32, dev),
+                                  _stream(dev, stream))
+    _check(rc, "pkv_paged_decode_run")
     return out
 
 

@@ -452,12 +452,17 @@ int max_resident(const void* fn) {
     return slot;
 }
 
+// How a decode's plan kernel is launched: ordinarily, as a programmatic
+// dependent of a kv_store just enqueued, or not at all (a plan already in the
+// workspace).
+enum class PlanLaunch { kPlain, kAfterStore, kNone };
+
 template <int D>
-int launch_decode(DecodeArgs& a, cudaStream_t s, bool after_store = false) {
-    if (after_store) {
+int launch_decode(DecodeArgs& a, cudaStream_t s, PlanLaunch plan = PlanLaunch::kPlain) {
+    if (plan == PlanLaunch::kAfterStore) {
         if (launch_dependent(decode_plan_kernel, dim3(1), dim3(1024), s, a) != cudaSuccess)
             return PKV_ERR_CUDA;
-    } else {
+    } else if (plan == PlanLaunch::kPlain) {
         decode_plan_kernel<<<1, 1024, 0, s>>>(a);
     }
     if (pkv_decode_tma_supported(a, D) == PKV_OK) {
@@ -499,6 +504,43 @@ extern "C" size_t pkv_paged_decode_workspace_bytes(int32_t batch, int32_t num_q_
 
 namespace {
 
+// Checks what the plan depends on (context lengths, sizes, workspace) and
+// fills the corresponding fields of `a`.
+int make_plan_args(const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                   int32_t max_context_len, int32_t max_blocks_per_seq, void* workspace,
+                   size_t workspace_bytes, const pkv_cache_desc& cache, uint32_t* status,
+                   DecodeArgs& a) {
+    if (batch < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || num_q_heads <= 0 ||
+        cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0)
+        return PKV_ERR_BAD_DIMENSION;
+    if (num_q_heads % cache.num_kv_heads != 0) return PKV_ERR_BAD_DIMENSION;
+    if (cache.head_dim != 64 && cache.head_dim != 128) return PKV_ERR_UNSUPPORTED_HEAD_DIM;
+    if (!context_lens || !workspace) return PKV_ERR_NULL_POINTER;
+    if ((uintptr_t)workspace & 15) return PKV_ERR_MISALIGNED;
+    if ((uintptr_t)context_lens & 3) return PKV_ERR_MISALIGNED;
+    const DecodeLayout L = decode_layout(batch, num_q_heads, max_context_len, cache);
+    if (workspace_bytes < L.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    char* ws = (char*)workspace;
+    a.ctx = context_lens;
+    a.chunk_prefix = (int32_t*)(ws + L.off_prefix);
+    a.chunk_info = (int4*)(ws + L.off_info);
+    a.part_ml = (float2*)(ws + L.off_ml);
+    a.part_o = (float*)(ws + L.off_o);
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cache.num_kv_heads;
+    a.G = num_q_heads / cache.num_kv_heads;
+    a.n_hg = (a.G + kMaxGroup - 1) / kMaxGroup;
+    a.MB = max_blocks_per_seq;
+    a.NB = cache.num_blocks;
+    a.bs = cache.block_size;
+    a.max_ctx = max_context_len;
+    a.chunk_keys = L.chunk_keys;
+    a.cap = L.cap;
+    a.status = status;
+    return PKV_OK;
+}
+
 // Checks the arguments and fills `a`; PKV_OK means the decode may be launched.
 int make_decode_args(const void* q, const void* k_cache, const void* v_cache,
                      const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -517,32 +559,16 @@ int make_decode_args(const void* q, const void* k_cache, const void* v_cache,
          (uintptr_t)workspace) & 15)
         return PKV_ERR_MISALIGNED;
     if (((uintptr_t)block_tables | (uintptr_t)context_lens) & 3) return PKV_ERR_MISALIGNED;
-    const DecodeLayout L = decode_layout(batch, num_q_heads, max_context_len, cache);
-    if (workspace_bytes < L.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
-    char* ws = (char*)workspace;
+    const int rc = make_plan_args(context_lens, batch, num_q_heads, max_context_len,
+                                  max_blocks_per_seq, workspace, workspace_bytes, cache, status,
+                                  a);
+    if (rc != PKV_OK) return rc;
     a.q = (const __nv_bfloat16*)q;
     a.kc = (const __nv_bfloat16*)k_cache;
     a.vc = (const __nv_bfloat16*)v_cache;
     a.bt = block_tables;
-    a.ctx = context_lens;
     a.out = (__nv_bfloat16*)out;
-    a.chunk_prefix = (int32_t*)(ws + L.off_prefix);
-    a.chunk_info = (int4*)(ws + L.off_info);
-    a.part_ml = (float2*)(ws + L.off_ml);
-    a.part_o = (float*)(ws + L.off_o);
-    a.B = batch;
-    a.Hq = num_q_heads;
-    a.Hkv = cache.num_kv_heads;
-    a.G = num_q_heads / cache.num_kv_heads;
-    a.n_hg = (a.G + kMaxGroup - 1) / kMaxGroup;
-    a.MB = max_blocks_per_seq;
-    a.NB = cache.num_blocks;
-    a.bs = cache.block_size;
-    a.max_ctx = max_context_len;
-    a.chunk_keys = L.chunk_keys;
-    a.cap = L.cap;
     a.scale_log2 = scale * pkv::kLog2e;
-    a.status = status;
     return PKV_OK;
 }
 
@@ -564,6 +590,38 @@ extern "C" int pkv_paged_decode(const void* q, const void* k_cache, const void* 
     return cache.head_dim == 128 ? launch_decode<128>(a, s) : launch_decode<64>(a, s);
 }
 
+extern "C" int pkv_paged_decode_plan(const int32_t* context_lens, int32_t batch,
+                                     int32_t num_q_heads, int32_t max_context_len,
+                                     int32_t max_blocks_per_seq, void* workspace,
+                                     size_t workspace_bytes, pkv_cache_desc cache,
+                                     uint32_t* status, void* stream) {
+    if (batch == 0 && max_context_len >= 0 && num_q_heads > 0) return PKV_OK;
+    DecodeArgs a{};
+    const int rc = make_plan_args(context_lens, batch, num_q_heads, max_context_len,
+                                  max_blocks_per_seq, workspace, workspace_bytes, cache, status,
+                                  a);
+    if (rc != PKV_OK) return rc;
+    decode_plan_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_paged_decode_run(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t batch,
+                                    int32_t num_q_heads, int32_t max_context_len, float scale,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    pkv_cache_desc cache, uint32_t* status, void* stream) {
+    if (batch == 0 && max_context_len >= 0 && num_q_heads > 0) return PKV_OK;
+    DecodeArgs a{};
+    const int rc = make_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    context_lens, batch, num_q_heads, max_context_len, scale, out,
+                                    workspace, workspace_bytes, cache, status, a);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    return cache.head_dim == 128 ? launch_decode<128>(a, s, PlanLaunch::kNone)
+                                 : launch_decode<64>(a, s, PlanLaunch::kNone);
+}
+
 extern "C" int pkv_kv_store_paged_decode(
         const void* k, const void* v, const int32_t* slot_mapping, int32_t num_tokens,
         const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
@@ -581,9 +639,10 @@ extern "C" int pkv_kv_store_paged_decode(
     rc = pkv_kv_store(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache, status, stream);
     if (rc != PKV_OK) return rc;                 // nothing enqueued
     cudaStream_t s = (cudaStream_t)stream;
-    const bool chained = num_tokens > 0;         // an empty store launches nothing
-    return cache.head_dim == 128 ? launch_decode<128>(a, s, chained)
-                                 : launch_decode<64>(a, s, chained);
+    // an empty store launches nothing
+    const PlanLaunch plan = num_tokens > 0 ? PlanLaunch::kAfterStore : PlanLaunch::kPlain;
+    return cache.head_dim == 128 ? launch_decode<128>(a, s, plan)
+                                 : launch_decode<64>(a, s, plan);
 }
 
 // ---------------------------------------------------------------------------

@@ -76,8 +76,15 @@ def test_host_checks_return_codes_without_a_gpu(lib):
     assert lib.pkv_kv_store_paged_prefill_varlen(None, None, None, None, None, None, None, None,
                                                  1, 4, 4, 4, 2, None, 0, 0.0, None, None, 0, c,
                                                  None, None) == -2
+    # the decode plan checks what it depends on
+    assert lib.pkv_paged_decode_plan(None, 2, 2, 8, 2, None, 0, c, None, None) == -1
+    assert lib.pkv_paged_decode_plan(None, 2, 2, 8, 2, None, 0, bad, None, None) == -3
+    assert lib.pkv_paged_decode_plan(None, 0, 2, 8, 2, None, 0, c, None, None) == 0
+    assert lib.pkv_paged_decode_run(None, None, None, None, 2, None, 2, 2, 8, 1.0, None, None,
+                                    0, c, None, None) == -1
     # a misaligned pointer is rejected on the host; it is never dereferenced
     p = ctypes.c_void_p(16 * 1024 + 2)
+    assert lib.pkv_paged_decode_plan(p, 2, 2, 8, 2, p, 1 << 20, c, None, None) == -4
     assert lib.pkv_sample(p, p, p, 1, 10, p, None, None) == -4
     assert lib.pkv_kv_store_paged_prefill_varlen(p, p, p, p, p, p, p, p, 1, 4, 4, 4, 2, None, 0,
                                                  1.0, p, p, 1 << 20, c, None, None) == -4

@@ -90,3 +90,71 @@ def test_decode_through_a_multi_layer_pool(cuda):
     a = pkv.paged_decode(w.q, kc, vc, bt, ctx, w.scale, w.max_context_len)
     b = pkv.paged_decode(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale, w.max_context_len)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("bs", [256, 16])
+def test_plan_once_run_per_layer(cuda, bs):
+    """pkv_paged_decode_plan once, then pkv_paged_decode_run for each layer of
+    a [2, L, NB, bs, Hkv, D] pool: each layer's output is exactly what
+    pkv_paged_decode gives, eagerly and replayed from one CUDA graph; a context
+    length the plan rejects is reported and its rows are zero."""
+    pkv = U.lib()
+    spec = W.DecodeSpec("plan-run", seed=31, batch=20, num_q_heads=16, num_kv_heads=4,
+                        head_dim=128, block_size=bs, ctx_lo=1, ctx_hi=1500)
+    w = W.decode_workload(spec, device=cuda)
+    L = 3
+    g = torch.Generator().manual_seed(5)
+    pool = torch.empty((2, L) + tuple(w.k_cache.shape), dtype=torch.bfloat16, device=cuda)
+    for layer in range(L):
+        pool[0, layer].copy_(torch.randn(w.k_cache.shape, generator=g).to(torch.bfloat16))
+        pool[1, layer].copy_(torch.randn(w.v_cache.shape, generator=g).to(torch.bfloat16))
+    layers = [pkv.layer_cache(pool, layer) for layer in range(L)]
+    bt, ctx = w.block_tables.to(cuda), w.context_lens.to(cuda)
+    max_ctx = w.max_context_len
+    refs = [pkv.paged_decode(w.q, kc, vc, bt, ctx, w.scale, max_ctx) for kc, vc in layers]
+    st = pkv.new_status(cuda)
+    ws = pkv.paged_decode_plan(ctx, spec.num_q_heads, max_ctx, bt.shape[1], layers[0][0],
+                               status=st)
+    outs = [pkv.paged_decode_run(w.q, kc, vc, bt, ctx, w.scale, max_ctx, ws, status=st)
+            for kc, vc in layers]
+    torch.cuda.synchronize()
+    assert U.status_word(st) == 0
+    for o, r in zip(outs, refs):
+        assert torch.equal(o, r)
+    # the same step captured in one graph
+    outs_g = [torch.empty_like(w.q) for _ in layers]
+
+    def step():
+        pkv.paged_decode_plan(ctx, spec.num_q_heads, max_ctx, bt.shape[1], layers[0][0],
+                              workspace=ws, status=st)
+        for (kc, vc), o in zip(layers, outs_g):
+            pkv.paged_decode_run(w.q, kc, vc, bt, ctx, w.scale, max_ctx, ws, out=o, status=st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for o in outs_g:
+        o.zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for o, r in zip(outs_g, refs):
+        assert torch.equal(o, r)
+    # a rejected context length: reported by the plan, zero rows from the run
+    bad = ctx.clone()
+    bad[3] = max_ctx + 1
+    st2 = pkv.new_status(cuda)
+    ws2 = pkv.paged_decode_plan(bad, spec.num_q_heads, max_ctx, bt.shape[1], layers[0][0],
+                                status=st2)
+    o2 = pkv.paged_decode_run(w.q, layers[0][0], layers[0][1], bt, bad, w.scale, max_ctx, ws2)
+    torch.cuda.synchronize()
+    assert U.status_word(st2) == pkv.STATUS["BAD_CONTEXT_LEN"]
+    assert float(o2[3].abs().max()) == 0.0
+    keep = [b for b in range(spec.batch) if b != 3]
+    assert torch.equal(o2[keep], refs[0][keep])

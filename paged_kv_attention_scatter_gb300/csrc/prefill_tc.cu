@@ -5,10 +5,11 @@
 // What it computes is stated in prefill.cu (causal varlen prefill over a
 // prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
 //
-// Work item = (sequence, 128-query tile, q head); the persistent grid walks
-// the cost-sorted tile list of the plan kernel (heads innermost, so the G
-// heads of a kv group read the same K/V tiles out of L2 at about the same
-// time).  The keys of a q tile are covered by
+// Work item = (sequence, 128-query tile, q head); the persistent grid takes
+// items of the plan kernel's cost-sorted list dynamically (the producer warp
+// draws the next index from a counter and hands it to the other roles
+// through a small ring in shared memory), heads innermost, so the G heads of
+// a kv group read the same K/V tiles out of L2 at about the same time.  The keys of a q tile are covered by
 //   * cached tiles u = 0 .. ceil(c/128)-1: keys 128u .. 128u+127 of the
 //     prefix, one TMA box per half of head_dim at row
 //     block_tables[b][128u / bs] * bs + (128u % bs) of the pool (a 128-key
@@ -65,6 +66,8 @@ constexpr int kTile = kBM * kD * 2;      // bytes of one bf16 128x128 tile
 constexpr int kHalf = kTile / 2;         // one 64-column half (128 rows x 128 B)
 constexpr int kThreads = 224;
 constexpr int kStages = 3;               // K/V ring depth
+constexpr int kItemRing = 4;             // work items handed from the producer to the others
+constexpr int kItemReaders = 6;          // Q K^T issuer, P V issuer, 4 softmax warps
 constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
 
@@ -76,6 +79,8 @@ struct __align__(1024) TcSmem {
     uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
     uint64_t s_full[kStages], p_full[kStages], pv_done[kStages];
     uint64_t o_free, mma_done;
+    uint64_t item_full[kItemRing], item_empty[kItemRing];
+    int32_t item_ring[kItemRing];        // item index, or -1 when the CTA is done
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -112,6 +117,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, r);
 }
 
+// Item I of this CTA from the producer's ring (-1: no more).  A whole warp
+// calls it when `warp_wide`, else one thread; the slot is released after the
+// read.
+__device__ __forceinline__ bool next_item(TcSmem& s, uint32_t I, int32_t& it,
+                                          bool warp_wide = false) {
+    const int qs = I % kItemRing;
+    const uint32_t par = (I / kItemRing) & 1;
+    const bool got = warp_wide ? warp_wait(&s.item_full[qs], par, &s.abort_flag)
+                               : mbar_wait(&s.item_full[qs], par, &s.abort_flag);
+    if (!got) return false;
+    it = s.item_ring[qs];
+    if (warp_wide) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&s.item_empty[qs]);
+    } else {
+        mbar_arrive(&s.item_empty[qs]);
+    }
+    return true;
+}
+
 __device__ __forceinline__ void give_up(TcSmem& s, uint32_t* status) {
     s.abort_flag = 1;
     pkv::report(status, PKV_STATUS_WAIT_TIMEOUT);
@@ -137,6 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             mbar_init(&s.pv_done[i], 1);
         }
         mbar_init(&s.o_free, 128);
+        for (int q = 0; q < kItemRing; ++q) {
+            mbar_init(&s.item_full[q], 1);
+            mbar_init(&s.item_empty[q], kItemReaders);
+        }
         mbar_init(&s.mma_done, 2);
         mbar_init_fence();
     }
@@ -161,7 +190,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             uint32_t T = 0, I = 0;
             bool ok = true, bad_block = false;
             const int32_t oob_row = a.NB * a.bs;   // past the pool: TMA fills zeros
-            for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
+            for (; ok; ++I) {
+                // the next item of the cost-sorted list, taken dynamically so
+                // the CTAs finish together; the other roles read it from the ring
+                const int qs = I % kItemRing;
+                if (I >= kItemRing &&
+                    !(ok = mbar_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1, &s.abort_flag)))
+                    break;
+                const int32_t it = atomicAdd(&a.sched[1], 1);
+                s.item_ring[qs] = it < n_items ? it : -1;
+                mbar_arrive(&s.item_full[qs]);
+                if (it >= n_items) break;
                 const Item x = item_at(a, it);
                 const int32_t kvh = x.h / a.G;
                 if (I > 0 && !(ok = mbar_wait(&s.q_free, (I - 1) & 1, &s.abort_flag))) break;
@@ -228,7 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             const uint64_t vd0 = umma_desc_sw128(saddr(s.v[0]), kHalf, 1024);
             uint32_t T = 0, I = 0;
             bool ok = true;
-            for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
+            for (; ok; ++I) {
+                int32_t it = -1;
+                if (!(ok = next_item(s, I, it))) break;
+                if (it < 0) break;
                 const Item x = item_at(a, it);
                 if (warp == 5) {
                     if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag))) break;
@@ -287,7 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         uint32_t T = 0, I = 0;
         bool ok = true;
-        for (int64_t it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++I) {
+        for (; ok; ++I) {
+            int32_t it = -1;
+            if (!(ok = next_item(s, I, it, true))) break;
+            if (it < 0) break;
             const Item x = item_at(a, it);
             float m_run = -INFINITY, l_run = 0.f;
             for (int32_t j = 0; j < x.n_tiles && ok; ++j) {

@@ -110,6 +110,13 @@ __device__ __forceinline__ Item item_at(const PrefillArgs& a, int64_t it) {
     return x;
 }
 
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // All 32 lanes wait on the same barrier; the result is made warp-uniform so
 // the warp-wide TMEM instructions that follow never see a diverged warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const int* abort_flag) {
@@ -355,20 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     lim = i + 1;
                     masked = true;
                 }
-                // eight independent partial maxima: no 128-long dependency chain
-                float mxp[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+                // eight independent partial maxima (no 128-long dependency
+                // chain), two new columns per three-input max
                 if (masked) {
 #pragma unroll
-                    for (int col = 0; col < kBN; ++col) {
-                        sv[col] = col < lim ? sv[col] : -INFINITY;
-                        mxp[col & 7] = fmaxf(mxp[col & 7], sv[col]);
-                    }
-                } else {
-#pragma unroll
-                    for (int col = 0; col < kBN; ++col) mxp[col & 7] = fmaxf(mxp[col & 7], sv[col]);
+                    for (int col = 0; col < kBN; ++col) sv[col] = col < lim ? sv[col] : -INFINITY;
                 }
+                float mxp[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mxp[e] = fmaxf(sv[e], sv[8 + e]);
+#pragma unroll
+                for (int col = 16; col < kBN; col += 16)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mxp[e] = max3(mxp[e], sv[col + e], sv[col + 8 + e]);
                 float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
                 mx *= a.scale_log2;                         // scale > 0 keeps the order

@@ -32,12 +32,12 @@ METRIC = "paged decode HBM GB/s (% of peak) & prefill tokens/s (% TC peak), 1 GB
 L2_BYTES = 129e6
 LAYERS_0P6B = 28                   # decoder layers of a Qwen3-0.6B-shaped model
 
-# DRAM bytes (read + write) of one decode-0.6b paged_decode call, summed over
-# its plan, split and combine launches, from one ncu capture (profiles/
+# DRAM bytes (read + write) of one decode-0.6b paged_decode_run, summed over
+# its split and combine launches, from one ncu capture (profiles/
 # decode_tma_kernel_decode-0.6b.md).  Valid only for the decode sources it was
 # taken on: the digest below must match, otherwise the traffic is reported null.
-DECODE_0P6B_TRAFFIC = {"bytes": 585880064,
-                       "sources_sha256": "41bb9ae96534c7e89bff247f03d4b1c0268897c3957fdc8e09ba90c256ff0d4e"}
+DECODE_0P6B_TRAFFIC = {"bytes": 585666816,
+                       "sources_sha256": "6393d2ba684c415798b95743dcc78efa2981a5e41d5f508c3e6d778a8b113b2f"}
 DECODE_SOURCES = ["paged_decode.cu", "paged_decode_tma.cu", "decode_common.cuh", "common.cuh",
                   "tc_utils.cuh", "tma_host.cuh"]
 
@@ -333,7 +333,7 @@ def run_ours(args, rank, world, dist):
                      "traffic": (DECODE_0P6B_TRAFFIC["bytes"]
                                  if decode_sources_digest() ==
                                  DECODE_0P6B_TRAFFIC["sources_sha256"] else None),
-                     "traffic_unit": "bytes per call", "peak_source": pk["source"],
+                     "traffic_unit": "bytes per paged_decode_run", "peak_source": pk["source"],
                      "kernel": "paged_decode_run (split-KV + combine launches), 28 per "
                                "step, plus one plan launch per step",
                      "bytes_per_launch": nbytes / LAYERS_0P6B},

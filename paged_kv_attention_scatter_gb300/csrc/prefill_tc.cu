@@ -1,6 +1,6 @@
 // paged_prefill_varlen on the 5th-generation tensor cores: tcgen05.mma with
 // TMEM accumulators, Q/K/V tiles staged by TMA, for head_dim 128 and block
-// sizes that are multiples of 128.
+// sizes that are multiples of 128 or one of 8, 16, 32, 64.
 //
 // What it computes is stated in prefill.cu (causal varlen prefill over a
 // prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
@@ -11,9 +11,10 @@
 // through a small ring in shared memory), heads innermost, so the G heads of
 // a kv group read the same K/V tiles out of L2 at about the same time.  The keys of a q tile are covered by
 //   * cached tiles u = 0 .. ceil(c/128)-1: keys 128u .. 128u+127 of the
-//     prefix, one TMA box per half of head_dim at row
-//     block_tables[b][128u / bs] * bs + (128u % bs) of the pool (a 128-key
-//     tile never crosses a block because bs is a multiple of 128);
+//     prefix, per half of head_dim one TMA box at row
+//     block_tables[b][128u / bs] * bs + (128u % bs) of the pool when bs is a
+//     multiple of 128, else 128/bs boxes of bs rows, one per block, stacked
+//     in shared memory (keys past the prefix read zeros);
 //   * new tiles t = 0 .. m: the chunk's own k/v rows q0 + 128t ..; tile t == m
 //     is the diagonal (causal mask col <= row), tiles t > m are never visible.
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
@@ -69,6 +70,7 @@ constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
 constexpr int kItemReaders = 6;          // Q K^T issuer, P V issuer, 4 softmax warps
 constexpr uint32_t kColS0 = 0, kColO = 384;
+constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
 
 struct __align__(1024) TcSmem {
@@ -149,6 +151,10 @@ __device__ __forceinline__ void give_up(TcSmem& s, uint32_t* status) {
     pkv::report(status, PKV_STATUS_WAIT_TIMEOUT);
 }
 
+// kBoxed: the pool's blocks hold fewer than 128 keys, so a cached tile is
+// gathered from 128/bs boxes (a separate instantiation keeps the common
+// one-box producer loop free of that code).
+template <bool kBoxed>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -197,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             uint32_t T = 0, I = 0;
             bool ok = true, bad_block = false;
             const int32_t oob_row = a.NB * a.bs;   // past the pool: TMA fills zeros
+            const int cache_box = kBoxed ? a.bs : kBN;
             for (; ok; ++I) {
                 // the next item of the cost-sorted list, taken dynamically so
                 // the CTAs finish together; the other roles read it from the ring
@@ -220,17 +227,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     const uint32_t use = T / kStages;
                     if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_flag)))
                         break;
+                    // a tile is one box of 128 rows, or (cached tiles of a pool with
+                    // blocks below 128 keys) one box per block, stacked
                     const CUtensorMap* mk;
                     const CUtensorMap* mv;
-                    int32_t row;
+                    int32_t row = oob_row;
+                    int32_t rows[kMaxBoxes];
+                    const bool boxed = kBoxed && j < x.n_cached;
                     if (j < x.n_cached) {
                         const int32_t key0 = j * kBN;
-                        const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
-                        if ((unsigned)blk < (unsigned)a.NB) {
-                            row = blk * a.bs + key0 % a.bs;
+                        if (!boxed) {
+                            const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
+                            if ((unsigned)blk < (unsigned)a.NB)
+                                row = blk * a.bs + key0 % a.bs;
+                            else
+                                bad_block = true;
                         } else {
-                            row = oob_row;
-                            bad_block = true;
+#pragma unroll
+                            for (int u = 0; u < kMaxBoxes; ++u) {
+                                rows[u] = oob_row;
+                                const int32_t key = key0 + u * cache_box;
+                                if (key < key0 + kBN && key < x.c) {   // past the prefix: zeros
+                                    const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
+                                    if ((unsigned)blk < (unsigned)a.NB)
+                                        rows[u] = blk * a.bs + key % a.bs;
+                                    else
+                                        bad_block = true;
+                                }
+                            }
                         }
                         mk = &maps.kc;
                         mv = &maps.vc;
@@ -240,15 +264,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         mv = &maps.v;
                     }
                     mbar_expect_tx(&s.k_full[st], kTile);
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(s.k[st] + hf * kHalf, mk, &s.k_full[st], hf * 64, kvh, row);
+                    if (!boxed) {
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_3d(s.k[st] + hf * kHalf, mk, &s.k_full[st], hf * 64, kvh, row);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < kMaxBoxes; ++u)
+                            if (u * cache_box < kBN)
+#pragma unroll
+                                for (int hf = 0; hf < 2; ++hf)
+                                    tma_load_3d(s.k[st] + hf * kHalf + u * cache_box * 128, mk,
+                                                &s.k_full[st], hf * 64, kvh, rows[u]);
+                    }
                     if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag))) {
                         mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
                         break;
                     }
                     mbar_expect_tx(&s.v_full[st], kTile);
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(s.v[st] + hf * kHalf, mv, &s.v_full[st], hf * 64, kvh, row);
+                    if (!boxed) {
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_3d(s.v[st] + hf * kHalf, mv, &s.v_full[st], hf * 64, kvh, row);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < kMaxBoxes; ++u)
+                            if (u * cache_box < kBN)
+#pragma unroll
+                                for (int hf = 0; hf < 2; ++hf)
+                                    tma_load_3d(s.v[st] + hf * kHalf + u * cache_box * 128, mv,
+                                                &s.v_full[st], hf * 64, kvh, rows[u]);
+                    }
                 }
             }
             if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
@@ -475,16 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 }
 
 // ---------------------------------------------------------------- host side
-// [rows, heads, 128] bf16, box 64 x 1 head x 128 rows.
-bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads) {
-    return pkv::tma_encode_rows(m, base, rows, heads, kD, 128);
+// [rows, heads, 128] bf16, box 64 x 1 head x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads,
+                 int box_rows = kBN) {
+    return pkv::tma_encode_rows(m, base, rows, heads, kD, box_rows);
 }
 
 }  // namespace
 
 int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
     if (head_dim != kD) return PKV_ERR_UNSUPPORTED;
-    if (a.bt != nullptr && (a.bs % kBN) != 0) return PKV_ERR_UNSUPPORTED;
+    if (a.bt != nullptr && a.bs % kBN != 0 && (a.bs % 8 != 0 || kBN % a.bs != 0))
+        return PKV_ERR_UNSUPPORTED;
     if ((int64_t)a.NB * a.bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
     if (pkv::tma_encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
@@ -497,20 +543,22 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue*
         !encode_rows(&maps.v, a.v, a.total_q, a.Hkv))
         return PKV_ERR_CUDA;
     if (a.bt) {
-        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv) ||
-            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv))
+        const int box = a.bs % kBN == 0 ? kBN : a.bs;
+        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, box) ||
+            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, box))
             return PKV_ERR_CUDA;
     } else {
         maps.kc = maps.k;
         maps.vc = maps.v;
     }
     const int smem = (int)sizeof(TcSmem) + 1024;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
+    const bool boxed = a.bt != nullptr && a.bs % kBN != 0;
+    static bool configured[2] = {false, false};
+    if (!configured[boxed]) {
+        if (cudaFuncSetAttribute(boxed ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return PKV_ERR_CUDA;
-        configured = true;
+        configured[boxed] = true;
     }
     a.tile_m = kBM;
     a.tile_n = kBN;
@@ -530,6 +578,8 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue*
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, prefill_tc_kernel, maps, a) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, boxed ? prefill_tc_kernel<true> : prefill_tc_kernel<false>, maps,
+                           a) != cudaSuccess)
+        return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -9,10 +9,14 @@
 //
 // Design for GB300 (HBM-bound: every cache byte is read once):
 //  * Work unit = (sequence, kv head, group of <= 8 q heads, chunk of keys).  A
-//    one-CTA plan kernel writes each sequence's chunk count as a prefix sum in
-//    the workspace; the persistent main grid (SMs x resident CTAs) walks the
-//    units round-robin, so empty units cost nothing and nothing depends on a
-//    host-side length (the launch is graph-capturable).
+//    one-CTA plan kernel writes each sequence's chunk count as a prefix sum,
+//    and one record per chunk (sequence, key range, chunk count), into the
+//    workspace; the persistent main grid (SMs x resident CTAs) walks the
+//    units round-robin, reading a unit's record with one load, so empty units
+//    cost nothing and nothing depends on a host-side length (the launch is
+//    graph-capturable).  Block sizes that are multiples of 64 take the TMA-fed
+//    split kernel of paged_decode_tma.cu; this file's split kernel takes the
+//    others.
 //  * Inside a unit each of the 4 warps takes 16-key steps.  K and V rows are
 //    loaded straight from HBM into mma.sync fragments with 16-byte loads (a
 //    warp reads 8 rows x 64 B of K and 4 rows x 128 B of V per instruction):
@@ -134,18 +138,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
         const int32_t sc = (int32_t)(u / units_per_sc);
         const int32_t rem = (int32_t)(u - (int64_t)sc * units_per_sc);
         const int32_t kvh = rem / a.n_hg, hg = rem - kvh * a.n_hg;
-        // sequence owning chunk slot sc: the last b with prefix[b] <= sc
-        int32_t lo = 0, hi = a.B;
-        while (lo < hi) {
-            const int32_t mid = (lo + hi + 1) >> 1;
-            if (a.chunk_prefix[mid] <= sc) lo = mid; else hi = mid - 1;
-        }
-        const int32_t b = lo;
-        const int32_t chunk = sc - a.chunk_prefix[b];
-        const int32_t nch = a.chunk_prefix[b + 1] - a.chunk_prefix[b];
-        const int32_t ctx = a.ctx[b];
-        const int32_t key0 = chunk * a.chunk_keys;
-        const int32_t key_end = min(ctx, key0 + a.chunk_keys);
+        // the plan's record of chunk slot sc: sequence, key range, chunk count
+        const int4 info = a.chunk_info[sc];
+        const int32_t b = info.x, key0 = info.y, key_end = info.z, nch = info.w;
         const int32_t h0 = kvh * a.G + hg * kMaxGroup;
         const int32_t nh = min(kMaxGroup, a.G - hg * kMaxGroup);
         const int32_t* bt_row = a.bt + (int64_t)b * a.MB;

@@ -9,7 +9,8 @@
 // no max, no exp, no sum -- each element costs one multiply, one log and one
 // compare, and the row is read exactly once (8 bytes per vocabulary entry).
 //
-// Design: a thread-block cluster of up to 8 CTAs owns one row; each CTA scans a
+// Design: a thread-block cluster of up to 8 CTAs owns one row at a time (as
+// many clusters as can be resident, each walking rows); each CTA scans a
 // contiguous segment with 16-byte streaming loads, reduces its best
 // (key, index) by warp shuffles and shared memory, and rank 0 of the cluster
 // gathers the CTAs' results over distributed shared memory.  Ties keep the
@@ -89,17 +90,19 @@ __device__ __forceinline__ uint32_t word_of(const uint4& w, int j) {
 template <bool kPhilox>
 __global__ void __launch_bounds__(kThreads) sample_kernel(
         const float* __restrict__ logits, const float* __restrict__ temperatures,
-        const float* __restrict__ noise, uint64_t seed, uint64_t offset, int32_t row0,
+        const float* __restrict__ noise, uint64_t seed, uint64_t offset, int32_t num_rows,
         int32_t vocab, bool vec_ok, int32_t* __restrict__ out, uint32_t* status) {
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int csize = (int)cluster.num_blocks();
-    const int64_t row = (int64_t)row0 + blockIdx.y;
 
     __shared__ float warp_key[kThreads / 32];
     __shared__ int warp_idx[kThreads / 32];
-    __shared__ Cand cta_best;
+    __shared__ Cand cta_best[2];          // by row parity: one cluster barrier per row
 
+    // persistent: a cluster per resident slot walks rows blockIdx.y, +gridDim.y, ...
+    int par = 0;
+    for (int64_t row = blockIdx.y; row < num_rows; row += gridDim.y, par ^= 1) {
     const float temp = temperatures[row];
     const bool t_ok = isfinite(temp) && temp > 0.f;
     Cand best{-CUDART_INF_F, INT_MAX};
@@ -116,7 +119,29 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
         if (vec_ok) {
             // rows start 16-byte aligned: lo is a multiple of 4 (and so is n_row)
             const int nvec = (hi - lo) >> 2;
-            for (int v = threadIdx.x; v < nvec; v += kThreads) {
+            int v0 = threadIdx.x;
+            if (!kPhilox) {
+                // four vectors of logits and noise in flight per thread: all
+                // loads issued before any key is compared
+                for (; v0 + 3 * kThreads < nvec; v0 += 4 * kThreads) {
+                    float4 l4[4], e4[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = lo + 4 * (v0 + u * kThreads);
+                        l4[u] = pkv::ld_stream16f(lrow + i);
+                        e4[u] = pkv::ld_stream16f(nrow + i);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = lo + 4 * (v0 + u * kThreads);
+                        take_if_better(best, gumbel_key(l4[u].x, inv_t, e4[u].x), i);
+                        take_if_better(best, gumbel_key(l4[u].y, inv_t, e4[u].y), i + 1);
+                        take_if_better(best, gumbel_key(l4[u].z, inv_t, e4[u].z), i + 2);
+                        take_if_better(best, gumbel_key(l4[u].w, inv_t, e4[u].w), i + 3);
+                    }
+                }
+            }
+            for (int v = v0; v < nvec; v += kThreads) {
                 const int i = lo + 4 * v;
                 const float4 l4 = pkv::ld_stream16f(lrow + i);
                 float4 e4;
@@ -165,13 +190,15 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
     if (threadIdx.x == 0) {
         Cand c{warp_key[0], warp_idx[0]};
         for (int w = 1; w < kThreads / 32; ++w) take_if_better(c, warp_key[w], warp_idx[w]);
-        cta_best = c;
+        cta_best[par] = c;
     }
-    cluster.sync();                       // every CTA's cta_best is written
+    // every CTA's cta_best[par] is written; the slot is written again two rows
+    // later, after the next barrier, which rank 0 reaches only once it has read it
+    cluster.sync();
     if (rank == 0 && threadIdx.x == 0) {
-        Cand c = cta_best;
+        Cand c = cta_best[par];
         for (int r = 1; r < csize; ++r) {
-            const Cand* other = cluster.map_shared_rank(&cta_best, r);
+            const Cand* other = cluster.map_shared_rank(&cta_best[par], r);
             take_if_better(c, other->key, other->idx);
         }
         int32_t tok = 0;
@@ -183,6 +210,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
             tok = c.idx;
         }
         out[row] = tok;
+    }
     }
     cluster.sync();                       // keep shared memory alive for rank 0
 }
@@ -201,20 +229,32 @@ int launch_sample(const float* logits, const float* temperatures, const float* e
     attr[0].val.clusterDim.x = (unsigned)csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    for (int32_t r0 = 0; r0 < batch; r0 += 65535) {
-        const int32_t rows = batch - r0 < 65535 ? batch - r0 : 65535;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)csize, (unsigned)rows, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = (cudaStream_t)stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel<kPhilox>, logits, temperatures,
-                                           exp_noise, seed, offset, r0, vocab, vec_ok,
-                                           out_token_ids, status);
-        if (e != cudaSuccess) return PKV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)csize, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = (cudaStream_t)stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many clusters as can be resident at once (no partial last wave),
+    // each walking rows; queried once per cluster size
+    static int resident[2][9] = {};
+    int& n_res = resident[kPhilox ? 1 : 0][csize];
+    if (n_res == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, sample_kernel<kPhilox>, &cfg) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = 65535;
+        }
+        n_res = n;
     }
+    const int32_t clusters = batch < n_res ? batch : n_res;
+    cfg.gridDim = dim3((unsigned)csize, (unsigned)clusters, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel<kPhilox>, logits, temperatures,
+                                       exp_noise, seed, offset, batch, vocab, vec_ok,
+                                       out_token_ids, status);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

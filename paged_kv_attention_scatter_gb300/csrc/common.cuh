@@ -5,7 +5,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pagedattn.h"
+
+// Raises a kernel's dynamic shared memory limit to `bytes` on the current
+// device, once per device (the attribute is per device, so one flag per
+// process would leave a second GPU of the same process unset).  `done` is the
+// call site's mask of devices already set.
+inline bool pkv_dynamic_smem_once(const void* fn, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return false;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return true;
+}
 
 namespace pkv {
 

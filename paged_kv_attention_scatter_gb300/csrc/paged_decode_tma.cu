@@ -424,13 +424,9 @@ int launch(DecodeArgs& a, cudaStream_t s) {
         !pkv::tma_encode_rows(&vmap, a.vc, rows, a.Hkv, D, kStageKeys))
         return PKV_ERR_CUDA;
     const int smem = (int)sizeof(DecodeSmem<D>) + 1024;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(decode_tma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    if (!pkv_dynamic_smem_once((const void*)decode_tma_kernel<D>, smem, configured))
+        return PKV_ERR_CUDA;
     int64_t grid = pkv_num_sms();
     const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;
     if (grid > upper) grid = upper;

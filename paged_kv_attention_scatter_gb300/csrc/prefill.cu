@@ -356,14 +356,9 @@ __global__ void __launch_bounds__(kThreadsG) prefill_general_kernel(PrefillArgs 
 template <int D>
 int launch_general(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre) {
     const size_t smem = (size_t)(kBM + 4 * kBN) * (D / 8) * 16;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(prefill_general_kernel<D>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};
+    if (!pkv_dynamic_smem_once((const void*)prefill_general_kernel<D>, (int)smem, configured))
+        return PKV_ERR_CUDA;
     a.tile_m = kBM;
     a.tile_n = kBN;
     const int rc = pkv_launch_prefill_plan(a, s, pre);

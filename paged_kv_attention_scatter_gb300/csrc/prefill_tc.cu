@@ -553,13 +553,11 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue*
     }
     const int smem = (int)sizeof(TcSmem) + 1024;
     const bool boxed = a.bt != nullptr && a.bs % kBN != 0;
-    static bool configured[2] = {false, false};
-    if (!configured[boxed]) {
-        if (cudaFuncSetAttribute(boxed ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured[boxed] = true;
-    }
+    static std::atomic<uint64_t> configured[2];
+    if (!pkv_dynamic_smem_once(boxed ? (const void*)prefill_tc_kernel<true>
+                                     : (const void*)prefill_tc_kernel<false>,
+                               smem, configured[boxed]))
+        return PKV_ERR_CUDA;
     a.tile_m = kBM;
     a.tile_n = kBN;
     const int rc = pkv_launch_prefill_plan(a, s, pre);

@@ -173,3 +173,58 @@ def test_stated_maximum_context_sets_the_chunking(cuda, max_ctx_scale):
     ref = oatt.paged_decode(U.f64(w.q), w.k_cache, w.v_cache, w.block_tables.numpy(),
                             w.context_lens.numpy(), w.scale)
     U.assert_close(U.f64(out), ref, f"decode, max_ctx x{max_ctx_scale}")
+
+
+def test_decode_0p6b_plan_and_layer_runs_in_a_graph(cuda):
+    """The headline's launch configuration at full size: one plan, then one run
+    per layer of a [2, L, NB, bs, Hkv, D] pool, all captured in one CUDA graph
+    and replayed.  Each layer holds its own random cache; every layer's output
+    is checked against the float64 oracle on a sample of sequences (the
+    shortest, the longest and a spread between)."""
+    pkv = U.lib()
+    spec = W.DECODE_0P6B
+    w = W.decode_workload(spec)
+    L = 3
+    g = torch.Generator().manual_seed(404)
+    pool = torch.empty((2, L) + tuple(w.k_cache.shape), dtype=torch.bfloat16)
+    for layer in range(L):
+        pool[0, layer] = torch.randn(w.k_cache.shape, generator=g).to(torch.bfloat16)
+        pool[1, layer] = torch.randn(w.v_cache.shape, generator=g).to(torch.bfloat16)
+    pool_d = pool.to(cuda)
+    layers = [pkv.layer_cache(pool_d, layer) for layer in range(L)]
+    q, bt, ctx = w.q.to(cuda), w.block_tables.to(cuda), w.context_lens.to(cuda)
+    mc, mb = w.max_context_len, bt.shape[1]
+    ws = torch.empty(pkv.paged_decode_workspace_bytes(spec.batch, spec.num_q_heads, mc,
+                                                      layers[0][0]),
+                     dtype=torch.uint8, device=cuda)
+    outs = [torch.zeros_like(q) for _ in range(L)]
+    st = pkv.new_status(cuda)
+
+    def step():
+        pkv.paged_decode_plan(ctx, spec.num_q_heads, mc, mb, layers[0][0], workspace=ws,
+                              status=st)
+        for (kc, vc), o in zip(layers, outs):
+            pkv.paged_decode_run(q, kc, vc, bt, ctx, w.scale, mc, ws, out=o, status=st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for o in outs:
+        o.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert U.status_word(st) == 0
+    order = np.argsort(w.context_lens.numpy())
+    seqs = sorted(set([int(order[0]), int(order[-1])] + [int(x) for x in order[::9]]))
+    for layer in range(L):
+        ref = oatt.paged_decode(U.f64(w.q), pool[0, layer], pool[1, layer],
+                                w.block_tables.numpy(), w.context_lens.numpy(), w.scale,
+                                seqs=seqs)
+        U.assert_close(U.f64(outs[layer])[seqs], ref[seqs], f"decode-0.6b layer {layer}")

@@ -330,34 +330,50 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
     }
 }
 
-constexpr int kCombineBatch = 8;     // chunks whose partials are loaded at once
-constexpr int kCombineHeads = 4;     // q heads per combine CTA
+constexpr int kCombineBatch = 16;    // chunks whose partials are loaded at once
+constexpr int kCombineHeads = 4;     // q heads per combine CTA, one warp each
 
-// One CTA per (sequence, 4 q heads), one thread per (head, head_dim element).
-// Each thread merges the chunks' partials of its element online, loading the
-// (max, sum) pairs and the partial outputs of up to 8 chunks at once, so the
-// whole merge is one round trip per 8 chunks with no block-wide reduction.
+// One warp per (sequence, q head); lane l owns head_dim elements
+// [l*D/32, (l+1)*D/32).  The chunks' (max, sum) pairs and partial outputs of up
+// to 16 chunks are loaded at once and merged online (base 2), so a sequence of
+// up to 16 chunks costs one round trip; no block-wide reduction.
 template <int D>
-__global__ void __launch_bounds__(D * kCombineHeads, 2) decode_combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(32 * kCombineHeads) decode_combine_kernel(DecodeArgs a) {
+    constexpr int E = D / 32;
     wait_for_predecessor();                  // the split kernel's partials
-    const int32_t h = blockIdx.x * kCombineHeads + threadIdx.y, b = blockIdx.y, d = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t h = blockIdx.x * kCombineHeads + warp, b = blockIdx.y;
     if (h >= a.Hq) return;
     const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
     if (n == 1) return;                                  // written by the split kernel
-    const int64_t qh = (int64_t)b * a.Hq + h;
-    float M = -INFINITY, L = 0.f, O = 0.f;
+    const int d0 = lane * E;
+    float M = -INFINITY, L = 0.f, O[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) O[e] = 0.f;
     for (int32_t c0 = 0; c0 < n; c0 += kCombineBatch) {
         const int cn = min(kCombineBatch, n - c0);
         float2 ml[kCombineBatch];
-        float ov[kCombineBatch];
+        float ov[kCombineBatch][E];
 #pragma unroll
         for (int c = 0; c < kCombineBatch; ++c) {
             ml[c] = make_float2(-INFINITY, 0.f);
-            ov[c] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) ov[c][e] = 0.f;
             if (c < cn) {
                 const int64_t slot = (int64_t)(p0 + c0 + c) * a.Hq + h;
                 ml[c] = a.part_ml[slot];
-                ov[c] = a.part_o[slot * D + d];
+                const float* po = a.part_o + slot * D + d0;
+                if constexpr (E == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(po);
+                    ov[c][0] = v.x;
+                    ov[c][1] = v.y;
+                    ov[c][2] = v.z;
+                    ov[c][3] = v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(po);
+                    ov[c][0] = v.x;
+                    ov[c][1] = v.y;
+                }
             }
         }
         float mb = M;
@@ -366,17 +382,23 @@ __global__ void __launch_bounds__(D * kCombineHeads, 2) decode_combine_kernel(De
         if (mb == -INFINITY) continue;                   // nothing visible yet
         const float r = (M == -INFINITY) ? 0.f : pkv::fast_exp2(M - mb);
         L *= r;
-        O *= r;
+#pragma unroll
+        for (int e = 0; e < E; ++e) O[e] *= r;
 #pragma unroll
         for (int c = 0; c < kCombineBatch; ++c) {
             if (ml[c].x == -INFINITY) continue;
             const float f = pkv::fast_exp2(ml[c].x - mb);
             L += ml[c].y * f;
-            O += ov[c] * f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) O[e] += ov[c][e] * f;
         }
         M = mb;
     }
-    a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    __nv_bfloat16* dst = a.out + ((int64_t)b * a.Hq + h) * D + d0;
+#pragma unroll
+    for (int e = 0; e < E; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + e) =
+            pkv::pack_bf16(L > 0.f ? O[e] / L : 0.f, L > 0.f ? O[e + 1] / L : 0.f);
 }
 
 template <typename... Args>
@@ -480,7 +502,7 @@ int launch_decode(DecodeArgs& a, cudaStream_t s, PlanLaunch plan = PlanLaunch::k
         sub.out = a.out + (int64_t)b0 * a.Hq * D;
         const unsigned hblocks = (unsigned)((a.Hq + kCombineHeads - 1) / kCombineHeads);
         if (launch_dependent(decode_combine_kernel<D>, dim3(hblocks, (unsigned)rows),
-                             dim3(D, kCombineHeads), s, sub) != cudaSuccess)
+                             dim3(32 * kCombineHeads), s, sub) != cudaSuccess)
             return PKV_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

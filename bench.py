@@ -2,11 +2,14 @@
 """Benchmark of the paged-KV attention hot path on GB300.
 
 Headline: paged decode HBM GB/s on the decode-0.6b workload (B=64, 16/8 heads,
-D=128, 256-slot blocks, context U[512,4096]); a step is one paged_decode call
-over the batch (plan + split-KV + combine kernels), replayed from a CUDA graph
-so host launch cost does not enter the device time.  The same JSON line also
-carries the prefill-8b chunked prefill (tokens/s, TFLOP/s, % of the tensor
-peak), decode-32b and the step-8b decode step as `secondary`.
+D=128, 256-slot blocks, context U[512,4096]); a step is the decode attention of
+a 28-layer Qwen3-0.6B-shaped model: one paged_decode_plan and 28
+paged_decode_run calls (split-KV + combine kernels) over a multi-layer pool,
+replayed from one CUDA graph so host launch cost does not enter the device
+time.  `e2e` is the same step through the public API with pinned host buffers
+copied in and out every step.  The same JSON line also carries the prefill-8b
+chunked prefill (tokens/s, TFLOP/s, % of the tensor peak), decode-32b, the
+step-8b decode step and a single call per graph launch as `secondary`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -264,23 +267,54 @@ def run_ours(args, rank, world, dist):
 
     # ---------------- e2e through the C ABI with host buffers ----------------
     # every step: block tables, context lengths and each layer's q copied in
-    # from pinned host memory, each layer's output read back
+    # from pinned host memory, each layer's output read back.  The copies run
+    # on two copy streams, ordered against the attention by events, so layer
+    # i+1's q arrives and layer i's output leaves while layer i+1 computes.
     q_h = q.cpu().pin_memory()
     bt_h, ctx_h = bt.cpu().pin_memory(), ctx.cpu().pin_memory()
     out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in layers]
     q_d = [torch.empty_like(q) for _ in layers]
     out_d = [torch.empty_like(out) for _ in layers]
-    bt_d, ctx_d = torch.empty_like(bt), torch.empty_like(ctx)
+    bt_d = [torch.empty_like(bt) for _ in range(2)]        # by step parity
+    ctx_d = [torch.empty_like(ctx) for _ in range(2)]
+    ws_d = [ws, torch.empty_like(ws)]
     e2e_steps = max(10, min(args.steps, 300))
+    ms = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    ev_meta, ev_step = ev(), [ev(), ev()]
+    ev_q = [ev() for _ in layers]
+    ev_run = [ev() for _ in layers]
+    ev_d2h = [ev() for _ in layers]
+    for e_ in ev_step + ev_run + ev_d2h:
+        e_.record(ms)
+    counter = [0]
 
     def e2e_step():
-        bt_d.copy_(bt_h, non_blocking=True)
-        ctx_d.copy_(ctx_h, non_blocking=True)
-        pkv.paged_decode_plan(ctx_d, hq, max_ctx, mb, layers[0][0], workspace=ws)
+        p = counter[0] & 1
+        counter[0] += 1
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(ev_step[p])          # the step two back is done with them
+            bt_d[p].copy_(bt_h, non_blocking=True)
+            ctx_d[p].copy_(ctx_h, non_blocking=True)
+            ev_meta.record(h2d_s)
+            for i in range(len(layers)):
+                h2d_s.wait_event(ev_run[i])       # the previous step's run i read q_d[i]
+                q_d[i].copy_(q_h, non_blocking=True)
+                ev_q[i].record(h2d_s)
+        ms.wait_event(ev_meta)
+        pkv.paged_decode_plan(ctx_d[p], hq, max_ctx, mb, layers[0][0], workspace=ws_d[p])
         for i, (kc, vc) in enumerate(layers):
-            q_d[i].copy_(q_h, non_blocking=True)
-            pkv.paged_decode_run(q_d[i], kc, vc, bt_d, ctx_d, scale, max_ctx, ws, out=out_d[i])
-            out_h[i].copy_(out_d[i], non_blocking=True)
+            ms.wait_event(ev_q[i])
+            ms.wait_event(ev_d2h[i])              # out_d[i] of the previous step was read
+            pkv.paged_decode_run(q_d[i], kc, vc, bt_d[p], ctx_d[p], scale, max_ctx, ws_d[p],
+                                 out=out_d[i])
+            ev_run[i].record(ms)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_run[i])
+                out_h[i].copy_(out_d[i], non_blocking=True)
+                ev_d2h[i].record(d2h_s)
+        ev_step[p].record(ms)
 
     for _ in range(max(3, args.warmup // 10)):
         e2e_step()
@@ -288,6 +322,7 @@ def run_ours(args, rank, world, dist):
     t0.record()
     for _ in range(e2e_steps):
         e2e_step()
+    ms.wait_stream(d2h_s)                         # the last outputs are on the host
     t1.record()
     torch.cuda.synchronize()
     e2e_s = t0.elapsed_time(t1) * 1e-3 / e2e_steps

@@ -419,7 +419,8 @@ int pkv_launch_prefill_plan(PrefillArgs& a, cudaStream_t s, const PrefillPrologu
 // tcgen05 fast path (prefill_tc.cu): returns PKV_ERR_UNSUPPORTED when the
 // shapes are not its own.
 int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim);
-int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre);
+int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
+                         const PrefillPrologue* pre);
 
 namespace {
 
@@ -480,7 +481,8 @@ int make_prefill_args(const void* q, const void* k, const void* v, const void* k
 }
 
 int launch_prefill(PrefillArgs& a, int head_dim, cudaStream_t s, const PrefillPrologue* pre) {
-    if (pkv_prefill_tc_supported(a, head_dim) == PKV_OK) return pkv_launch_prefill_tc(a, s, pre);
+    if (pkv_prefill_tc_supported(a, head_dim) == PKV_OK)
+        return pkv_launch_prefill_tc(a, head_dim, s, pre);
     return head_dim == 128 ? launch_general<128>(a, s, pre) : launch_general<64>(a, s, pre);
 }
 

@@ -1,6 +1,6 @@
 // paged_prefill_varlen on the 5th-generation tensor cores: tcgen05.mma with
-// TMEM accumulators, Q/K/V tiles staged by TMA, for head_dim 128 and block
-// sizes that are multiples of 128 or one of 8, 16, 32, 64.
+// TMEM accumulators, Q/K/V tiles staged by TMA, for head_dim 128 or 64 and
+// block sizes that are multiples of 128 or one of 8, 16, 32, 64.
 //
 // What it computes is stated in prefill.cu (causal varlen prefill over a
 // prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
@@ -62,9 +62,9 @@ namespace {
 
 constexpr int kBM = 128;                 // queries per tile
 constexpr int kBN = 128;                 // keys per tile
-constexpr int kD = 128;                  // head_dim
-constexpr int kTile = kBM * kD * 2;      // bytes of one bf16 128x128 tile
-constexpr int kHalf = kTile / 2;         // one 64-column half (128 rows x 128 B)
+// head_dim D is 128 or 64: a tile is D/64 column blocks of 64 bf16 (one
+// 128-byte swizzle atom wide), each 128 rows x 128 B
+constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
 constexpr int kThreads = 224;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
@@ -73,7 +73,9 @@ constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
 
+template <int D>
 struct __align__(1024) TcSmem {
+    static constexpr int kTile = kBM * D * 2;     // bytes of one bf16 tile
     unsigned char q[kTile];
     unsigned char k[kStages][kTile];
     unsigned char v[kStages][kTile];
@@ -129,7 +131,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // Item I of this CTA from the producer's ring (-1: no more).  A whole warp
 // calls it when `warp_wide`, else one thread; the slot is released after the
 // read.
-__device__ __forceinline__ bool next_item(TcSmem& s, uint32_t I, int32_t& it,
+template <class Smem>
+__device__ __forceinline__ bool next_item(Smem& s, uint32_t I, int32_t& it,
                                           bool warp_wide = false) {
     const int qs = I % kItemRing;
     const uint32_t par = (I / kItemRing) & 1;
@@ -146,7 +149,8 @@ __device__ __forceinline__ bool next_item(TcSmem& s, uint32_t I, int32_t& it,
     return true;
 }
 
-__device__ __forceinline__ void give_up(TcSmem& s, uint32_t* status) {
+template <class Smem>
+__device__ __forceinline__ void give_up(Smem& s, uint32_t* status) {
     s.abort_flag = 1;
     pkv::report(status, PKV_STATUS_WAIT_TIMEOUT);
 }
@@ -154,11 +158,14 @@ __device__ __forceinline__ void give_up(TcSmem& s, uint32_t* status) {
 // kBoxed: the pool's blocks hold fewer than 128 keys, so a cached tile is
 // gathered from 128/bs boxes (a separate instantiation keeps the common
 // one-box producer loop free of that code).
-template <bool kBoxed>
+template <int D, bool kBoxed>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
+    constexpr int kTile = TcSmem<D>::kTile;
+    constexpr int kBlocks = D / 64;               // 64-column blocks of a tile
     extern __shared__ unsigned char smem_raw[];
-    TcSmem& s = *reinterpret_cast<TcSmem*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    TcSmem<D>& s =
+        *reinterpret_cast<TcSmem<D>*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 const int32_t kvh = x.h / a.G;
                 if (I > 0 && !(ok = mbar_wait(&s.q_free, (I - 1) & 1, &s.abort_flag))) break;
                 mbar_expect_tx(&s.q_full, kTile);
-                for (int hf = 0; hf < 2; ++hf)
+                for (int hf = 0; hf < kBlocks; ++hf)
                     tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
                                 x.q0 + x.m * kBM);
                 for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
@@ -265,14 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     }
                     mbar_expect_tx(&s.k_full[st], kTile);
                     if (!boxed) {
-                        for (int hf = 0; hf < 2; ++hf)
+                        for (int hf = 0; hf < kBlocks; ++hf)
                             tma_load_3d(s.k[st] + hf * kHalf, mk, &s.k_full[st], hf * 64, kvh, row);
                     } else {
 #pragma unroll
                         for (int u = 0; u < kMaxBoxes; ++u)
                             if (u * cache_box < kBN)
 #pragma unroll
-                                for (int hf = 0; hf < 2; ++hf)
+                                for (int hf = 0; hf < kBlocks; ++hf)
                                     tma_load_3d(s.k[st] + hf * kHalf + u * cache_box * 128, mk,
                                                 &s.k_full[st], hf * 64, kvh, rows[u]);
                     }
@@ -282,14 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     }
                     mbar_expect_tx(&s.v_full[st], kTile);
                     if (!boxed) {
-                        for (int hf = 0; hf < 2; ++hf)
+                        for (int hf = 0; hf < kBlocks; ++hf)
                             tma_load_3d(s.v[st] + hf * kHalf, mv, &s.v_full[st], hf * 64, kvh, row);
                     } else {
 #pragma unroll
                         for (int u = 0; u < kMaxBoxes; ++u)
                             if (u * cache_box < kBN)
 #pragma unroll
-                                for (int hf = 0; hf < 2; ++hf)
+                                for (int hf = 0; hf < kBlocks; ++hf)
                                     tma_load_3d(s.v[st] + hf * kHalf + u * cache_box * 128, mv,
                                                 &s.v_full[st], hf * 64, kvh, rows[u]);
                     }
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         // overlap the MMAs of the other, so the tensor pipe stays fed
         if (lane == 0) {
             const uint32_t id_qk = umma_idesc_bf16(kBM, kBN, false);
-            const uint32_t id_pv = umma_idesc_bf16(kBM, kD, true);
+            const uint32_t id_pv = umma_idesc_bf16(kBM, D, true);
             const uint64_t qd0 = umma_desc_sw128(saddr(s.q), 16, 1024);
             const uint64_t kd0 = umma_desc_sw128(saddr(s.k[0]), 16, 1024);
             const uint64_t vd0 = umma_desc_sw128(saddr(s.v[0]), kHalf, 1024);
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         const uint64_t kd = kd0 + (uint64_t)(st * (kTile >> 4));
                         const uint32_t d_s = tmem + kColS0 + st * kBN;
 #pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk) {
+                        for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
                             umma_bf16(d_s, qd0 + off, kd + off, id_qk, kk > 0);
                         }
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         break;
                     tc_fence_after();
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
                         float ov[32];
                         tmem_ld32(lane_base + kColO + cc * 32, ov);
                         tmem_wait_ld();
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     if (!(ok = warp_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
                     if (i >= lim) {
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf)
+                        for (int hf = 0; hf < kBlocks; ++hf)
 #pragma unroll
                             for (int qc = 0; qc < 8; ++qc)
                                 *reinterpret_cast<uint4*>(s.v[st] + hf * kHalf + i * 128 + qc * 16) =
@@ -487,9 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            __nv_bfloat16* orow = a.out + ((int64_t)(x.q0 + x.m * kBM + i) * a.Hq + x.h) * kD;
+            __nv_bfloat16* orow = a.out + ((int64_t)(x.q0 + x.m * kBM + i) * a.Hq + x.h) * D;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 float ov[32];
                 tmem_ld32(lane_base + kColO + cc * 32, ov);
                 tmem_wait_ld();
@@ -519,43 +526,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 }
 
 // ---------------------------------------------------------------- host side
-// [rows, heads, 128] bf16, box 64 x 1 head x box_rows rows.
-bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads,
+// [rows, heads, D] bf16, box 64 x 1 head x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int head_dim,
                  int box_rows = kBN) {
-    return pkv::tma_encode_rows(m, base, rows, heads, kD, box_rows);
+    return pkv::tma_encode_rows(m, base, rows, heads, head_dim, box_rows);
 }
 
-}  // namespace
-
-int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
-    if (head_dim != kD) return PKV_ERR_UNSUPPORTED;
-    if (a.bt != nullptr && a.bs % kBN != 0 && (a.bs % 8 != 0 || kBN % a.bs != 0))
-        return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)a.NB * a.bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
-    if (pkv::tma_encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
-    return PKV_OK;
-}
-
-int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre) {
-    TcMaps maps;
-    if (!encode_rows(&maps.q, a.q, a.total_q, a.Hq) ||
-        !encode_rows(&maps.k, a.k, a.total_q, a.Hkv) ||
-        !encode_rows(&maps.v, a.v, a.total_q, a.Hkv))
-        return PKV_ERR_CUDA;
-    if (a.bt) {
-        const int box = a.bs % kBN == 0 ? kBN : a.bs;
-        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, box) ||
-            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, box))
-            return PKV_ERR_CUDA;
-    } else {
-        maps.kc = maps.k;
-        maps.vc = maps.v;
-    }
-    const int smem = (int)sizeof(TcSmem) + 1024;
+template <int D>
+int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillPrologue* pre) {
+    const int smem = (int)sizeof(TcSmem<D>) + 1024;
     const bool boxed = a.bt != nullptr && a.bs % kBN != 0;
     static std::atomic<uint64_t> configured[2];
-    if (!pkv_dynamic_smem_once(boxed ? (const void*)prefill_tc_kernel<true>
-                                     : (const void*)prefill_tc_kernel<false>,
+    if (!pkv_dynamic_smem_once(boxed ? (const void*)prefill_tc_kernel<D, true>
+                                     : (const void*)prefill_tc_kernel<D, false>,
                                smem, configured[boxed]))
         return PKV_ERR_CUDA;
     a.tile_m = kBM;
@@ -576,8 +559,38 @@ int pkv_launch_prefill_tc(PrefillArgs& a, cudaStream_t s, const PrefillPrologue*
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, boxed ? prefill_tc_kernel<true> : prefill_tc_kernel<false>, maps,
-                           a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, boxed ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>,
+                           maps, a) != cudaSuccess)
         return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
+    if (head_dim != 128 && head_dim != 64) return PKV_ERR_UNSUPPORTED;
+    if (a.bt != nullptr && a.bs % kBN != 0 && (a.bs % 8 != 0 || kBN % a.bs != 0))
+        return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)a.NB * a.bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
+    if (pkv::tma_encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
+                         const PrefillPrologue* pre) {
+    TcMaps maps;
+    if (!encode_rows(&maps.q, a.q, a.total_q, a.Hq, head_dim) ||
+        !encode_rows(&maps.k, a.k, a.total_q, a.Hkv, head_dim) ||
+        !encode_rows(&maps.v, a.v, a.total_q, a.Hkv, head_dim))
+        return PKV_ERR_CUDA;
+    if (a.bt) {
+        const int box = a.bs % kBN == 0 ? kBN : a.bs;
+        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, box) ||
+            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, box))
+            return PKV_ERR_CUDA;
+    } else {
+        maps.kc = maps.k;
+        maps.vc = maps.v;
+    }
+    return head_dim == 128 ? launch_tc<128>(a, maps, s, pre) : launch_tc<64>(a, maps, s, pre);
 }

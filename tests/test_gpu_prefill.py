@@ -72,11 +72,12 @@ def test_tiny_with_and_without_block_tables(cuda):
     assert torch.equal(outs[0], outs[1])
 
 
-# head_dim 128 with block sizes 8..64 or multiples of 128 runs the tcgen05 kernel (several
-# TMA boxes per 128-key tile below 128); the others run the general kernel
+# head_dim 128 or 64 with block sizes 8..64 or multiples of 128 runs the tcgen05 kernel
+# (several TMA boxes per 128-key tile below 128); the others run the general kernel
 @pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 16), (4, 1, 64, 4), (6, 3, 128, 256),
                                          (2, 2, 64, 256), (16, 4, 128, 128), (8, 2, 128, 8),
-                                         (4, 4, 128, 32), (8, 1, 128, 64), (4, 2, 128, 48)])
+                                         (4, 4, 128, 32), (8, 1, 128, 64), (4, 2, 128, 48),
+                                         (4, 2, 64, 128), (8, 4, 64, 32), (6, 2, 64, 48)])
 def test_ragged_cached_prefixes(cuda, hq, hkv, d, bs):
     pkv = U.lib()
     lens = [200, 1, 129, 64, 300]

@@ -9,7 +9,8 @@ replayed from one CUDA graph so host launch cost does not enter the device
 time.  `e2e` is the same step through the public API with pinned host buffers
 copied in and out every step.  The same JSON line also carries the prefill-8b
 chunked prefill (tokens/s, TFLOP/s, % of the tensor peak), decode-32b, the
-step-8b decode step and a single call per graph launch as `secondary`.
+step-8b decode step, the mixed-8b continuous-batching step (decode rows and
+prefill chunks in one call) and a single call per graph launch as `secondary`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -397,7 +398,60 @@ def run_secondary(args, pkv, W, torch, dev, pk):
         res.update(bench_sample(pkv, W, torch, dev, pk))
     if "kvstore" in which:
         res.update(bench_kvstore(pkv, W, torch, dev, pk, flush))
+    if "mixed" in which:
+        res.update(bench_mixed(pkv, W, torch, dev, pk))
     return res
+
+
+def bench_mixed(pkv, W, torch, dev, pk):
+    """A continuous-batching layer step (mixed-8b): 256 decode rows and 4
+    prefill chunks in one varlen batch, stored and attended by one call that
+    routes the one-query rows to the decode kernels, against the same batch
+    through the prefill kernels alone.  The lower bound adds the decode rows'
+    bytes at the HBM peak to the chunks' flops at the tensor peak (the two
+    passes run one after the other)."""
+    spec = W.MIXED_8B
+    w = W.mixed_workload(spec, device=dev)
+    st = w.step
+    kc, vc = w.k_cache0, w.v_cache0
+    cu_q, cu_k = st.cu_seqlens_q.to(dev), st.cu_seqlens_k.to(dev)
+    bt, sl = st.block_tables.to(dev), st.slot_mapping.to(dev)
+    out = torch.empty_like(st.q)
+    B, T = st.cu_seqlens_q.numel() - 1, st.q.shape[0]
+    ws_m = torch.empty(pkv.paged_attention_varlen_workspace_bytes(
+        B, T, spec.num_q_heads, st.max_seqlen_k, kc.shape), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(pkv.paged_prefill_workspace_bytes(B, T, spec.num_q_heads, kc.shape),
+                       dtype=torch.uint8, device=dev)
+    gm = graph_of(lambda: pkv.kv_store_paged_attention_varlen(
+        st.q, st.k, st.v, kc, vc, sl, cu_q, cu_k, st.max_seqlen_q, st.max_seqlen_k, bt,
+        w.scale, out=out, workspace=ws_m), torch)
+    gp = graph_of(lambda: pkv.kv_store_paged_prefill_varlen(
+        st.q, st.k, st.v, kc, vc, sl, cu_q, cu_k, st.max_seqlen_q, st.max_seqlen_k, bt,
+        w.scale, out=out, workspace=ws_p), torch)
+    for g in (gm, gp):
+        for _ in range(3):
+            g.replay()
+    t_m, t_p = time_graph(gm, 20, torch), time_graph(gp, 20, torch)
+    lq = [b - a for a, b in zip(st.cu_seqlens_q.tolist(), st.cu_seqlens_q.tolist()[1:])]
+    lk = [b - a for a, b in zip(st.cu_seqlens_k.tolist(), st.cu_seqlens_k.tolist()[1:])]
+    dec_ctx = [k for q, k in zip(lq, lk) if q == 1]
+    b_dec = decode_bytes(dec_ctx, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                         spec.block_size)
+    pre = [(q, k) for q, k in zip(lq, lk) if q != 1]
+    cq = [0]
+    ck = [0]
+    for q, k in pre:
+        cq.append(cq[-1] + q)
+        ck.append(ck[-1] + k)
+    flops = prefill_flops(cq, ck, spec.num_q_heads, spec.head_dim)
+    t_lb = b_dec / (pk["hbm"] * 1e9) + flops / (pk["tc"] * 1e12)
+    return {"mixed-8b": {
+        "workload": spec.name, "decode_rows": len(dec_ctx), "prefill_tokens": sum(cq[-1:]),
+        "mixed_call_us": round(t_m * 1e6, 2), "all_prefill_call_us": round(t_p * 1e6, 2),
+        "speedup_vs_all_prefill": round(t_p / t_m, 3),
+        "lower_bound_us": round(t_lb * 1e6, 2), "frac_of_lower_bound": round(t_lb / t_m, 4),
+        "timing": "CUDA graph replays of one call (store + attention), CUDA events; the "
+                  "store re-writes the same slots"}}
 
 
 def bench_sample(pkv, W, torch, dev, pk):
@@ -557,6 +611,10 @@ def bench_step(pkv, W, torch, dev, pk):
     gd = graph_of(lambda: pkv.paged_decode(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale,
                                            w.max_context_len, out=out, workspace=ws), torch)
     gm = graph_of(lambda: pkv.sample(logits, temps, noise, out=ids), torch)
+    gz = graph_of(lambda: pkv.kv_store_paged_decode(w.k_new, w.v_new, sl, w.q, w.k_cache,
+                                                    w.v_cache, bt, ctx, w.scale,
+                                                    w.max_context_len, out=out, workspace=ws),
+                  torch)
 
     def full():
         pkv.kv_store(w.k_new, w.v_new, w.k_cache, w.v_cache, sl)
@@ -564,11 +622,12 @@ def bench_step(pkv, W, torch, dev, pk):
                          out=out, workspace=ws)
         pkv.sample(logits, temps, noise, out=ids)
     gf = graph_of(full, torch)
-    for gg in (gs, gd, gm, gf):
+    for gg in (gs, gd, gm, gf, gz):
         for _ in range(3):
             gg.replay()
     t_s, t_d, t_m, t_f = (time_graph(gs, 200, torch), time_graph(gd, 30, torch),
                           time_graph(gm, 50, torch), time_graph(gf, 30, torch))
+    t_z = time_graph(gz, 30, torch)
     b_s = 4.0 * w.k_new.numel() * 2
     b_d = decode_bytes(w.context_lens.tolist(), spec.num_q_heads, spec.num_kv_heads,
                        spec.head_dim, spec.block_size)
@@ -578,6 +637,7 @@ def bench_step(pkv, W, torch, dev, pk):
         "kv_store_us": round(t_s * 1e6, 2), "kv_store_gbs": round(b_s / t_s / 1e9, 1),
         "decode_us": round(t_d * 1e6, 2), "decode_gbs": round(b_d / t_d / 1e9, 1),
         "decode_frac_hbm": round(b_d / t_d / 1e9 / pk["hbm"], 4),
+        "fused_store_decode_us": round(t_z * 1e6, 2),
         "sample_us": round(t_m * 1e6, 2), "sample_gbs": round(b_m / t_m / 1e9, 1),
         "sample_frac_hbm": round(b_m / t_m / 1e9 / pk["hbm"], 4),
         "timing": "CUDA graph replays, CUDA events; kv_store re-writes the same slots"}
@@ -694,9 +754,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
-    ap.add_argument("--secondary", default="prefill,decode32,step",
+    ap.add_argument("--secondary", default="prefill,decode32,step,mixed",
                     help="comma list of secondary workloads: prefill, decode32, step, "
-                         "sample, kvstore")
+                         "mixed, sample, kvstore")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-worker", action="store_true")
     ap.add_argument("--per-step", type=int, default=1)

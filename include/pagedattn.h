@@ -300,6 +300,44 @@ PKV_API int pkv_kv_store_paged_prefill_varlen(
     void* stream);
 
 /*
+ * Bytes of device workspace pkv_kv_store_paged_attention_varlen needs (pure
+ * host function): the prefill's tile schedule followed by the decode's chunk
+ * plan and partial results, the latter sized for max_seqlen_k keys.
+ */
+PKV_API size_t pkv_paged_attention_varlen_workspace_bytes(int32_t batch, int32_t total_q,
+                                                  int32_t num_q_heads, int32_t max_seqlen_k,
+                                                  pkv_cache_desc cache);
+
+/*
+ * kv_store then attention over a mixed batch: prefill chunks and decode
+ * tokens in one step.  The pages' scheduler never mixes the two ([LIFE] §3.2),
+ * but a step's sequences each compute num_scheduled_tokens tokens from
+ * num_cached_tokens on ([LIFE] §3.1), so a decode row is a chunk of one token
+ * and continuous batching ([UML] §2.1) can take both in one call.  The
+ * arguments and the result are those of pkv_kv_store_paged_prefill_varlen
+ * (bottom-right causal attention of every query row), computed in two passes:
+ * sequences with Lq != 1 by the varlen prefill kernels, sequences with Lq == 1
+ * by the split-KV decode kernels.  The second pass reads all Lk keys of a
+ * one-query sequence from the cache through block_tables[b], its own key
+ * included, so slot_mapping must store that row at position Lk-1 of
+ * block_tables[b] (as an engine's slot mapping does); block_tables and the
+ * cache are required.
+ *   workspace     device, >= pkv_paged_attention_varlen_workspace_bytes(...)
+ *                 bytes, 16-byte aligned
+ * A one-query sequence whose lengths are inconsistent (Lk < 1, its row outside
+ * q, more keys than max_seqlen_k or than its table holds) sets
+ * PKV_STATUS_BAD_SEQLENS and its output row is not written.  Every argument
+ * is checked before anything is enqueued.
+ */
+PKV_API int pkv_kv_store_paged_attention_varlen(
+    const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+    const int32_t* slot_mapping, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+    int32_t batch, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+    int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq, float scale,
+    void* out, void* workspace, size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status,
+    void* stream);
+
+/*
  * sample -- temperature, softmax and Gumbel-max sampling of one token per row
  * ([UML] §2.4: "温度、softmax和gumbel max"; [LIFE] §4: the sampler runs on each
  * sequence's last-position logits).  With supplied Exp(1) noise E the draw is

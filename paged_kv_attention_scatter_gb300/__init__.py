@@ -12,8 +12,9 @@ ctypes binding:
 PyTorch supplies device memory and streams only.  `workloads` draws the seeded
 synthetic inputs the tests and the benchmark use.
 """
-from ._binding import (STATUS, cache_desc, kv_store, kv_store_paged_decode,  # noqa: F401
-                       kv_store_paged_prefill_varlen, layer_cache, library_path, load,
+from ._binding import (STATUS, cache_desc, kv_store, kv_store_paged_attention_varlen,  # noqa: F401,E501
+                       kv_store_paged_decode, kv_store_paged_prefill_varlen,
+                       paged_attention_varlen_workspace_bytes, layer_cache, library_path, load,
                        new_status, paged_decode, paged_decode_plan, paged_decode_run,
                        paged_decode_workspace_bytes, paged_prefill_varlen,
                        paged_prefill_workspace_bytes, sample, sample_philox, status_names)
@@ -21,6 +22,7 @@ from ._build import build  # noqa: F401
 
 __all__ = ["kv_store", "paged_decode", "paged_prefill_varlen", "sample", "build", "load",
            "kv_store_paged_decode", "kv_store_paged_prefill_varlen", "layer_cache",
+           "kv_store_paged_attention_varlen", "paged_attention_varlen_workspace_bytes",
            "paged_decode_plan", "paged_decode_run", "sample_philox",
            "paged_decode_workspace_bytes", "paged_prefill_workspace_bytes", "new_status",
            "status_names", "STATUS", "cache_desc", "library_path"]

@@ -34,7 +34,8 @@ C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_s
                "pkv_paged_prefill_workspace_bytes", "pkv_paged_prefill_varlen", "pkv_sample",
                "pkv_paged_decode_static_workspace", "pkv_kv_store_paged_decode",
                "pkv_kv_store_paged_prefill_varlen", "pkv_paged_decode_plan",
-               "pkv_paged_decode_run",
+               "pkv_paged_decode_run", "pkv_paged_attention_varlen_workspace_bytes",
+               "pkv_kv_store_paged_attention_varlen",
                "pkv_layer_cache", "pkv_sample_philox"]
 
 # Size of the scratch array compiled into the library for
@@ -95,6 +96,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pkv_kv_store_paged_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32,
                                                       I32, I32, P, I32, F32, P, P, SZ,
                                                       CacheDesc, P, P]
+    lib.pkv_paged_attention_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.pkv_paged_attention_varlen_workspace_bytes.argtypes = [I32, I32, I32, I32, CacheDesc]
+    lib.pkv_kv_store_paged_attention_varlen.restype = ctypes.c_int
+    lib.pkv_kv_store_paged_attention_varlen.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32,
+                                                        I32, I32, P, I32, F32, P, P, SZ,
+                                                        CacheDesc, P, P]
     lib.pkv_sample_philox.restype = ctypes.c_int
     lib.pkv_sample_philox.argtypes = [P, P, ctypes.c_uint64, ctypes.c_uint64, I32, I32, P, P, P]
     lib.pkv_layer_cache.restype = ctypes.c_int
@@ -321,6 +328,51 @@ def kv_store_paged_prefill_varlen(q, k, v, k_cache, v_cache, slot_mapping, cu_se
         workspace.numel(), cache_desc(k_cache), _ptr_or_null(status, "status", torch.int32, dev),
         _stream(dev, stream))
     _check(rc, "pkv_kv_store_paged_prefill_varlen")
+    return out
+
+
+def paged_attention_varlen_workspace_bytes(batch, total_q, num_q_heads, max_seqlen_k,
+                                           k_cache_shape) -> int:
+    nb, bs, hkv, d = k_cache_shape
+    return int(load().pkv_paged_attention_varlen_workspace_bytes(
+        batch, total_q, num_q_heads, int(max_seqlen_k), CacheDesc(nb, bs, hkv, d)))
+
+
+def kv_store_paged_attention_varlen(q, k, v, k_cache, v_cache, slot_mapping, cu_seqlens_q,
+                                    cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_tables,
+                                    scale, out=None, workspace=None, status=None,
+                                    stream=None) -> torch.Tensor:
+    """kv_store then attention over a batch mixing prefill chunks and decode
+    rows: the result of kv_store_paged_prefill_varlen, with one-query
+    sequences run by the split-KV decode kernels (they read their own new key
+    back from the cache, so slot_mapping must place it in their block table).
+    block_tables is required."""
+    lib = load()
+    dev = q.device
+    T, Hq, D = q.shape
+    B = cu_seqlens_q.numel() - 1
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must hold one slot per query token")
+    if block_tables is None:
+        raise ValueError("block_tables is required")
+    if out is None:
+        out = torch.empty_like(q)
+    need = paged_attention_varlen_workspace_bytes(B, T, Hq, max_seqlen_k, tuple(k_cache.shape))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib.pkv_kv_store_paged_attention_varlen(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k, "k", torch.bfloat16, dev),
+        _dev(v, "v", torch.bfloat16, dev), _dev(k_cache, "k_cache", torch.bfloat16, dev),
+        _dev(v_cache, "v_cache", torch.bfloat16, dev),
+        _dev(slot_mapping, "slot_mapping", torch.int32, dev),
+        _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev),
+        _dev(cu_seqlens_k, "cu_seqlens_k", torch.int32, dev), B, T, int(max_seqlen_q),
+        int(max_seqlen_k), Hq, _dev(block_tables, "block_tables", torch.int32, dev),
+        block_tables.shape[1], float(scale),
+        _dev(out, "out", torch.bfloat16, dev), _dev(workspace, "workspace", torch.uint8, dev),
+        workspace.numel(), cache_desc(k_cache), _ptr_or_null(status, "status", torch.int32, dev),
+        _stream(dev, stream))
+    _check(rc, "pkv_kv_store_paged_attention_varlen")
     return out
 
 

@@ -24,7 +24,20 @@ struct DecodeArgs {
     int32_t B, Hq, Hkv, G, n_hg, MB, NB, bs, max_ctx, chunk_keys, cap;
     float scale_log2;
     uint32_t* status;
+    // A varlen batch (mixed prefill and decode): when cu_q is set, sequence b
+    // is a decode row only if cu_q[b+1] - cu_q[b] == 1; its q and out row is
+    // cu_q[b] and its context cu_k[b+1] - cu_k[b].  Other sequences get no
+    // chunks and their out rows are left alone.
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int32_t total_q;                 // rows of q / out (varlen batch only)
+    int32_t b0;                      // first sequence of a combine launch
 };
+
+// q / out row of sequence b
+__device__ __forceinline__ int64_t row_of(const DecodeArgs& a, int32_t b) {
+    return a.cu_q != nullptr ? (int64_t)a.cu_q[b] : (int64_t)b;
+}
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;

@@ -43,6 +43,7 @@
 //  * Keys past ctx_b are never loaded (their registers are zero and their
 //    scores -inf), so NaN in unused cache slots cannot reach the output.
 #include "decode_common.cuh"
+#include "prefill_common.cuh"
 
 namespace {
 
@@ -67,12 +68,25 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
     for (int32_t base = 0; base < a.B; base += blockDim.x) {
         const int32_t b = base + threadIdx.x;
         int32_t n = 0;
+        int32_t c = 0;
         if (b < a.B) {
-            const int32_t c = a.ctx[b];
-            if (c < 0 || c > cap_keys || c > a.max_ctx) {
-                pkv::report(a.status, PKV_STATUS_BAD_CONTEXT_LEN);
+            if (a.cu_q != nullptr) {
+                // varlen batch: one-query rows only, with the prefill's checks
+                // (query row inside q, at least its own key, blocks inside the table)
+                const int32_t q0 = a.cu_q[b];
+                c = a.cu_k[b + 1] - a.cu_k[b];
+                if (a.cu_q[b + 1] - q0 == 1) {
+                    if (q0 < 0 || q0 >= a.total_q || c < 1 || c > cap_keys || c > a.max_ctx)
+                        pkv::report(a.status, PKV_STATUS_BAD_SEQLENS);
+                    else
+                        n = (c + a.chunk_keys - 1) / a.chunk_keys;
+                }
             } else {
-                n = (c + a.chunk_keys - 1) / a.chunk_keys;
+                c = a.ctx[b];
+                if (c < 0 || c > cap_keys || c > a.max_ctx)
+                    pkv::report(a.status, PKV_STATUS_BAD_CONTEXT_LEN);
+                else
+                    n = (c + a.chunk_keys - 1) / a.chunk_keys;
             }
         }
         // block-wide inclusive scan of n
@@ -99,7 +113,6 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
         if (b < a.B) {
             a.chunk_prefix[b + 1] = incl;
             // one record per chunk: what the split kernels need to start it
-            const int32_t c = n > 0 ? a.ctx[b] : 0;
             for (int32_t i = 0; i < n; ++i)
                 a.chunk_info[incl - n + i] =
                     make_int4(b, i * a.chunk_keys, min(c, (i + 1) * a.chunk_keys), n);
@@ -154,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
             qv[i] = make_uint4(0, 0, 0, 0);
             if (g < nh)
                 qv[i] = *reinterpret_cast<const uint4*>(
-                    a.q + ((int64_t)b * a.Hq + h0 + g) * D + (i * 4 + t) * 8);
+                    a.q + (pkv::row_of(a, b) * a.Hq + h0 + g) * D + (i * 4 + t) * 8);
         }
         float o[MT][4];
 #pragma unroll
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
                     O += sm_o[w][h][d] * f;
                 }
             }
-            const int64_t qh = (int64_t)b * a.Hq + h0 + h;
+            const int64_t qh = pkv::row_of(a, b) * a.Hq + h0 + h;
             if (nch == 1) {
                 a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
             } else {
@@ -342,10 +355,11 @@ __global__ void __launch_bounds__(32 * kCombineHeads) decode_combine_kernel(Deco
     constexpr int E = D / 32;
     wait_for_predecessor();                  // the split kernel's partials
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int32_t h = blockIdx.x * kCombineHeads + warp, b = blockIdx.y;
+    const int32_t h = blockIdx.x * kCombineHeads + warp, b = a.b0 + (int32_t)blockIdx.y;
     if (h >= a.Hq) return;
     const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
     if (n == 1) return;                                  // written by the split kernel
+    if (n == 0 && a.cu_q != nullptr) return;             // not a decode row of a varlen batch
     const int d0 = lane * E;
     float M = -INFINITY, L = 0.f, O[E];
 #pragma unroll
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(32 * kCombineHeads) decode_combine_kernel(Deco
         }
         M = mb;
     }
-    __nv_bfloat16* dst = a.out + ((int64_t)b * a.Hq + h) * D + d0;
+    __nv_bfloat16* dst = a.out + (pkv::row_of(a, b) * a.Hq + h) * D + d0;
 #pragma unroll
     for (int e = 0; e < E; e += 2)
         *reinterpret_cast<uint32_t*>(dst + e) =
@@ -498,8 +512,7 @@ int launch_decode(DecodeArgs& a, cudaStream_t s, PlanLaunch plan = PlanLaunch::k
     for (int32_t b0 = 0; b0 < a.B; b0 += 65535) {
         DecodeArgs sub = a;
         const int32_t rows = a.B - b0 < 65535 ? a.B - b0 : 65535;
-        sub.chunk_prefix = a.chunk_prefix + b0;
-        sub.out = a.out + (int64_t)b0 * a.Hq * D;
+        sub.b0 = b0;
         const unsigned hblocks = (unsigned)((a.Hq + kCombineHeads - 1) / kCombineHeads);
         if (launch_dependent(decode_combine_kernel<D>, dim3(hblocks, (unsigned)rows),
                              dim3(32 * kCombineHeads), s, sub) != cudaSuccess)
@@ -555,6 +568,10 @@ int make_plan_args(const int32_t* context_lens, int32_t batch, int32_t num_q_hea
     a.chunk_keys = L.chunk_keys;
     a.cap = L.cap;
     a.status = status;
+    a.cu_q = nullptr;
+    a.cu_k = nullptr;
+    a.total_q = 0;
+    a.b0 = 0;
     return PKV_OK;
 }
 
@@ -723,4 +740,86 @@ extern "C" int pkv_paged_decode_static_workspace(
     return pkv_paged_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                             batch, num_q_heads, max_context_len, scale, out, scratch,
                             (size_t)PKV_STATIC_DECODE_WORKSPACE_BYTES, cache, status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Mixed prefill and decode batches (continuous batching).
+//
+// A step of a continuous-batching engine carries prefill chunks and decode
+// rows in one varlen batch.  The causal varlen prefill computes every row
+// correctly, but a one-query sequence would take a whole 128-query tile (and
+// one CTA's worth of K/V streaming per head group); routing those rows to the
+// split-KV decode kernels gives them the decode path's parallelism and
+// bandwidth instead.  Order on the stream: the store, the prefill plan (its
+// programmatic dependent) and kernel over the multi-query sequences, then the
+// decode plan, split and combine over the one-query sequences.  The two sets
+// of rows are disjoint, so neither pass touches the other's output.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct MixedLayout {
+    size_t off_decode, total;
+};
+
+MixedLayout mixed_layout(int32_t batch, int32_t total_q, int32_t num_q_heads,
+                         int32_t max_seqlen_k, const pkv_cache_desc& c) {
+    MixedLayout L{};
+    const size_t pre = pkv_paged_prefill_workspace_bytes(batch, total_q, num_q_heads, c);
+    L.off_decode = (pre + 255) & ~(size_t)255;
+    L.total = L.off_decode + decode_layout(batch, num_q_heads, max_seqlen_k, c).total;
+    return L;
+}
+
+}  // namespace
+
+extern "C" size_t pkv_paged_attention_varlen_workspace_bytes(int32_t batch, int32_t total_q,
+                                                             int32_t num_q_heads,
+                                                             int32_t max_seqlen_k,
+                                                             pkv_cache_desc cache) {
+    if (batch < 0 || total_q < 0 || num_q_heads <= 0 || max_seqlen_k < 0 ||
+        cache.num_kv_heads <= 0 || cache.head_dim <= 0)
+        return 0;
+    return mixed_layout(batch, total_q, num_q_heads, max_seqlen_k, cache).total;
+}
+
+extern "C" int pkv_kv_store_paged_attention_varlen(
+        const void* q, const void* k, const void* v, void* k_cache, void* v_cache,
+        const int32_t* slot_mapping, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+        int32_t batch, int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+        int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+        float scale, void* out, void* workspace, size_t workspace_bytes, pkv_cache_desc cache,
+        uint32_t* status, void* stream) {
+    pkv::PrefillArgs p;
+    int rc = pkv_prefill_make_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, batch,
+                                   total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
+                                   block_tables, max_blocks_per_seq, scale, out, workspace,
+                                   workspace_bytes, cache, status, p);
+    if (rc != PKV_OK) return rc;                              // nothing enqueued
+    pkv::StoreCall store{k, v, k_cache, v_cache, slot_mapping, total_q, cache, status, stream};
+    if (batch == 0 || total_q == 0) {
+        bool launched = false;
+        return pkv_enqueue_store(&store, &launched);
+    }
+    // one-query sequences read every key, their own included, from the cache
+    if (!block_tables || !k_cache || !v_cache) return PKV_ERR_NULL_POINTER;
+    const MixedLayout L = mixed_layout(batch, total_q, num_q_heads, max_seqlen_k, cache);
+    if (workspace_bytes < L.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    DecodeArgs d{};
+    // cu_seqlens_k stands in for context_lens in the checks; the plan reads
+    // the lengths from cu_seqlens_q/k below.
+    rc = make_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_seqlens_k,
+                          batch, num_q_heads, max_seqlen_k, scale, out,
+                          (char*)workspace + L.off_decode, L.total - L.off_decode, cache, status,
+                          d);
+    if (rc != PKV_OK) return rc;
+    d.ctx = nullptr;
+    d.cu_q = cu_seqlens_q;
+    d.cu_k = cu_seqlens_k;
+    d.total_q = total_q;
+    p.skip_single = 1;
+    cudaStream_t s = (cudaStream_t)stream;
+    const PrefillPrologue pre{pkv_enqueue_store, &store};
+    rc = pkv_prefill_launch(p, cache.head_dim, s, &pre);
+    if (rc != PKV_OK) return rc;
+    return cache.head_dim == 128 ? launch_decode<128>(d, s) : launch_decode<64>(d, s);
 }

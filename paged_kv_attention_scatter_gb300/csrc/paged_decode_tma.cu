@@ -97,7 +97,16 @@ __device__ __forceinline__ int key_row(int k) { return k ^ ((k & 1) << 2); }
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
-template <int D>
+// q / out row of sequence b: b itself, or cu_q[b] in a varlen batch.  A
+// template flag rather than a run-time test: the test alone, in the producer
+// and the merge, cost the ordinary decode about 4%.
+template <bool kVarlen>
+__device__ __forceinline__ int64_t qrow_of(const DecodeArgs& a, int32_t b) {
+    if constexpr (kVarlen) return (int64_t)a.cu_q[b];
+    return (int64_t)b;
+}
+
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tma_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, DecodeArgs a) {
@@ -151,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t my_blk = lane < nblk ? a.bt[(int64_t)b * a.MB + blk0 + lane] : -1;
             const int32_t h0 = kvh * a.G + hg * kMaxGroup;
             const int32_t nh = min(kMaxGroup, a.G - hg * kMaxGroup);
+            const int64_t qrow = qrow_of<kVarlen>(a, b);
             for (int32_t k = key0; k < key_end; k += kStageKeys) {
                 if (!tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag)) {
                     ok = false;
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (first)
-                            bulk_load(sm.qs[slot], a.q + ((int64_t)b * a.Hq + h0) * D,
+                            bulk_load(sm.qs[slot], a.q + (qrow * a.Hq + h0) * D,
                                       (uint32_t)(nh * D * 2), &sm.full[slot]);
                     }
                 }
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     O += sm.o[w][h][d] * f;
                 }
             }
-            const int64_t qh = (int64_t)st.b * a.Hq + st.h0 + h;
+            const int64_t qh = qrow_of<kVarlen>(a, st.b) * a.Hq + st.h0 + h;
             if (st.nch == 1) {
                 a.out[qh * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
             } else {
@@ -424,8 +434,11 @@ int launch(DecodeArgs& a, cudaStream_t s) {
         !pkv::tma_encode_rows(&vmap, a.vc, rows, a.Hkv, D, kStageKeys))
         return PKV_ERR_CUDA;
     const int smem = (int)sizeof(DecodeSmem<D>) + 1024;
-    static std::atomic<uint64_t> configured{0};
-    if (!pkv_dynamic_smem_once((const void*)decode_tma_kernel<D>, smem, configured))
+    static std::atomic<uint64_t> configured[2] = {0, 0};
+    const bool varlen = a.cu_q != nullptr;
+    void (*kernel)(const CUtensorMap, const CUtensorMap, DecodeArgs) =
+        varlen ? decode_tma_kernel<D, true> : decode_tma_kernel<D, false>;
+    if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[varlen ? 1 : 0]))
         return PKV_ERR_CUDA;
     int64_t grid = pkv_num_sms();
     const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;
@@ -441,7 +454,7 @@ int launch(DecodeArgs& a, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, decode_tma_kernel<D>, kmap, vmap, a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, kmap, vmap, a) != cudaSuccess)
         return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

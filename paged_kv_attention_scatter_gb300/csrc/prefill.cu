@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
     for (int32_t b = w; b < a.B; b += nwarps) {
         int32_t q0, lq, lk;
         if (!pkv::seq_lengths(a, b, q0, lq, lk, lane == 0)) continue;
+        if (a.skip_single && lq == 1) continue;      // a decode row, attended elsewhere
         if (lane == 0 && (lq > a.max_sq || lk > a.max_sk))
             pkv::report(a.status, PKV_STATUS_BAD_SEQLENS);
         const int32_t c = lk - lq;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
     for (int32_t b = w; b < a.B; b += nwarps) {
         int32_t q0, lq, lk;
         if (!pkv::seq_lengths(a, b, q0, lq, lk, false)) continue;
+        if (a.skip_single && lq == 1) continue;
         const int32_t c = lk - lq;
         const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
         for (int32_t m = lane; m < nt; m += 32) {
@@ -424,8 +426,10 @@ int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
 
 namespace {
 
+}  // namespace
+
 // Checks every argument and fills the kernel arguments; enqueues nothing.
-int make_prefill_args(const void* q, const void* k, const void* v, const void* k_cache,
+int pkv_prefill_make_args(const void* q, const void* k, const void* v, const void* k_cache,
                       const void* v_cache, const int32_t* cu_seqlens_q,
                       const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
                       int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
@@ -477,36 +481,22 @@ int make_prefill_args(const void* q, const void* k, const void* v, const void* k
     a.max_tiles = L.max_tiles;
     a.scale_log2 = scale * pkv::kLog2e;
     a.status = status;
+    a.skip_single = 0;
     return PKV_OK;
 }
 
-int launch_prefill(PrefillArgs& a, int head_dim, cudaStream_t s, const PrefillPrologue* pre) {
+int pkv_prefill_launch(PrefillArgs& a, int head_dim, cudaStream_t s, const PrefillPrologue* pre) {
     if (pkv_prefill_tc_supported(a, head_dim) == PKV_OK)
         return pkv_launch_prefill_tc(a, head_dim, s, pre);
     return head_dim == 128 ? launch_general<128>(a, s, pre) : launch_general<64>(a, s, pre);
 }
 
-// The chunk's kv_store, run as the prologue of a fused prefill.
-struct StoreCall {
-    const void* k;
-    const void* v;
-    void* k_cache;
-    void* v_cache;
-    const int32_t* slot_mapping;
-    int32_t num_tokens;
-    pkv_cache_desc cache;
-    uint32_t* status;
-    void* stream;
-};
-
-int enqueue_store(void* ctx, bool* launched) {
-    const StoreCall& c = *(const StoreCall*)ctx;
+int pkv_enqueue_store(void* ctx, bool* launched) {
+    const pkv::StoreCall& c = *(const pkv::StoreCall*)ctx;
     *launched = c.num_tokens > 0;                 // an empty store launches nothing
     return pkv_kv_store(c.k, c.v, c.k_cache, c.v_cache, c.slot_mapping, c.num_tokens, c.cache,
                         c.status, c.stream);
 }
-
-}  // namespace
 
 extern "C" size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,
                                                     int32_t num_q_heads, pkv_cache_desc cache) {
@@ -524,12 +514,12 @@ extern "C" int pkv_paged_prefill_varlen(
         void* workspace, size_t workspace_bytes, pkv_cache_desc cache, uint32_t* status,
         void* stream) {
     PrefillArgs a;
-    const int rc = make_prefill_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+    const int rc = pkv_prefill_make_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
                                      batch, total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
                                      block_tables, max_blocks_per_seq, scale, out, workspace,
                                      workspace_bytes, cache, status, a);
     if (rc != PKV_OK || batch == 0 || total_q == 0) return rc;
-    return launch_prefill(a, cache.head_dim, (cudaStream_t)stream, nullptr);
+    return pkv_prefill_launch(a, cache.head_dim, (cudaStream_t)stream, nullptr);
 }
 
 extern "C" int pkv_kv_store_paged_prefill_varlen(
@@ -540,16 +530,16 @@ extern "C" int pkv_kv_store_paged_prefill_varlen(
         float scale, void* out, void* workspace, size_t workspace_bytes, pkv_cache_desc cache,
         uint32_t* status, void* stream) {
     PrefillArgs a;
-    const int rc = make_prefill_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+    const int rc = pkv_prefill_make_args(q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
                                      batch, total_q, max_seqlen_q, max_seqlen_k, num_q_heads,
                                      block_tables, max_blocks_per_seq, scale, out, workspace,
                                      workspace_bytes, cache, status, a);
     if (rc != PKV_OK) return rc;                              // nothing enqueued
-    StoreCall store{k, v, k_cache, v_cache, slot_mapping, total_q, cache, status, stream};
+    pkv::StoreCall store{k, v, k_cache, v_cache, slot_mapping, total_q, cache, status, stream};
     if (batch == 0 || total_q == 0) {
         bool launched = false;
-        return enqueue_store(&store, &launched);
+        return pkv_enqueue_store(&store, &launched);
     }
-    const PrefillPrologue pre{enqueue_store, &store};
-    return launch_prefill(a, cache.head_dim, (cudaStream_t)stream, &pre);
+    const PrefillPrologue pre{pkv_enqueue_store, &store};
+    return pkv_prefill_launch(a, cache.head_dim, (cudaStream_t)stream, &pre);
 }

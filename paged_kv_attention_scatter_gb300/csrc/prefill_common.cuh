@@ -21,6 +21,7 @@ struct PrefillArgs {
     int32_t tile_m, tile_n;          // tile shape the schedule is built for
     float scale_log2;
     uint32_t* status;
+    int32_t skip_single;             // sequences of one query are left to the decode kernels
 };
 
 // Lengths of sequence b; returns false (and reports) when they are inconsistent.
@@ -57,3 +58,35 @@ struct PrefillPrologue {
 
 // Enqueues `pre` (may be null), then the tile plan.
 int pkv_launch_prefill_plan(pkv::PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre);
+
+// Checks pkv_paged_prefill_varlen's arguments and fills `a` (enqueues nothing),
+// and enqueues `pre` (may be null) then the prefill of `a`; used by the entry
+// points that add a kv_store or decode rows around a prefill.
+int pkv_prefill_make_args(const void* q, const void* k, const void* v, const void* k_cache,
+                          const void* v_cache, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq, float scale,
+                          void* out, void* workspace, size_t workspace_bytes,
+                          pkv_cache_desc cache, uint32_t* status, pkv::PrefillArgs& a);
+int pkv_prefill_launch(pkv::PrefillArgs& a, int head_dim, cudaStream_t s,
+                       const PrefillPrologue* pre);
+
+namespace pkv {
+// A kv_store to run as the prologue of a fused call (its arguments, as
+// pkv_kv_store takes them).
+struct StoreCall {
+    const void* k;
+    const void* v;
+    void* k_cache;
+    void* v_cache;
+    const int32_t* slot_mapping;
+    int32_t num_tokens;
+    pkv_cache_desc cache;
+    uint32_t* status;
+    void* stream;
+};
+}  // namespace pkv
+
+// PrefillPrologue::enqueue for a pkv::StoreCall.
+int pkv_enqueue_store(void* store_call, bool* launched);

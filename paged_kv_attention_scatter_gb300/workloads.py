@@ -16,6 +16,8 @@ The shapes follow the five synthetic workloads (Qwen3-shaped attention layers):
   decode-32b    B=256, 64/8 heads, ctx log-uniform in [128, 32768], pool 7000
   step-8b       B=512, 32/8 heads, ctx ~ U[256, 8192]; kv_store of the new
                 token, decode, sampler over vocab 151936
+  mixed-8b      a continuous-batching step: 256 decode rows (ctx ~ U[256, 8192])
+                and 4 prefill chunks in one varlen batch, 32/8 heads
 
 Conventions (all choices of the input recipe, not of the method):
   * workload n uses seed n-1; integer draws are inclusive-uniform;
@@ -368,6 +370,90 @@ def prefill_workload(spec: PrefillSpec, device="cpu",
     return PrefillWorkload(spec=spec, prompt_lens=prompt_lens, cached_blocks=cached_blocks,
                            block_tables=tables, k_cache0=k0, v_cache0=v0, steps=steps,
                            scale=1.0 / math.sqrt(d))
+
+
+# ----------------------------------------------------------------------------
+# a continuous-batching step: decode rows and prefill chunks together
+# ----------------------------------------------------------------------------
+@dataclass(frozen=True)
+class MixedSpec:
+    name: str
+    seed: int
+    num_decode: int                    # one-query sequences
+    num_prefill: int                   # prefill chunks
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    ctx_lo: int                        # decode context, the new token included
+    ctx_hi: int
+    new_lo: int                        # new tokens of a prefill chunk
+    new_hi: int
+    cached_lo: int                     # tokens of a chunk's sequence already cached
+    cached_hi: int
+
+
+MIXED_8B = MixedSpec("mixed-8b 256 decode rows ctx U[256,8192] + 4 chunks of U[512,2048] "
+                     "new tokens on U[0,4096] cached, 32/8x128 bs256", seed=5,
+                     num_decode=256, num_prefill=4, num_q_heads=32, num_kv_heads=8,
+                     head_dim=128, block_size=256, ctx_lo=256, ctx_hi=8192,
+                     new_lo=512, new_hi=2048, cached_lo=0, cached_hi=4096)
+
+
+@dataclass
+class MixedWorkload:
+    spec: MixedSpec
+    step: PrefillStep               # the varlen batch, decode rows first
+    k_cache0: torch.Tensor          # pool before the step: cached tokens filled
+    v_cache0: torch.Tensor
+    scale: float
+
+
+def mixed_workload(spec: MixedSpec, device="cpu") -> MixedWorkload:
+    """One step of a batch that mixes decode rows (one new token on ctx-1
+    cached ones) with prefill chunks (new tokens on a cached prefix), in one
+    varlen batch; every sequence owns its blocks, and the step's slot_mapping
+    places each new token at its position in its own block table."""
+    g = _gen(spec.seed)
+    gdev = _gen(spec.seed, device)
+    bs, hq, hkv, d = spec.block_size, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    ctx = randint_incl(spec.ctx_lo, spec.ctx_hi, spec.num_decode, g)
+    new = randint_incl(spec.new_lo, spec.new_hi, spec.num_prefill, g)
+    cached = randint_incl(spec.cached_lo, spec.cached_hi, spec.num_prefill, g)
+    seqs = [(1, c - 1) for c in ctx] + list(zip(new, cached))    # (new, cached)
+    need = [ceil_div(n + c, bs) for n, c in seqs]
+    nb = sum(need)
+    perm = torch.randperm(nb, generator=g).tolist()
+    tables, at = [], 0
+    for n in need:
+        tables.append(perm[at:at + n])
+        at += n
+    valid = []
+    for t, (_, c) in zip(tables, seqs):
+        for i, blk in enumerate(t):
+            used = min(bs, c - i * bs)
+            if used > 0:
+                valid.append((blk, used))
+    k0 = fill_pool(nb, bs, hkv, d, valid, gdev, device)
+    v0 = fill_pool(nb, bs, hkv, d, valid, gdev, device)
+    T = sum(n for n, _ in seqs)
+    q = randn_bf16((T, hq, d), gdev, device)
+    k = randn_bf16((T, hkv, d), gdev, device)
+    v = randn_bf16((T, hkv, d), gdev, device)
+    cu_q, cu_k, slots = [0], [0], []
+    for t, (n, c) in zip(tables, seqs):
+        cu_q.append(cu_q[-1] + n)
+        cu_k.append(cu_k[-1] + c + n)
+        slots += slot_list(t, bs, c, n)
+    step = PrefillStep(q=q, k=k, v=v, cu_seqlens_q=torch.tensor(cu_q, dtype=torch.int32),
+                       cu_seqlens_k=torch.tensor(cu_k, dtype=torch.int32),
+                       block_tables=pad_tables(tables),
+                       slot_mapping=torch.tensor(slots, dtype=torch.int32),
+                       seq_ids=list(range(len(seqs))), q_start=[c for _, c in seqs],
+                       max_seqlen_q=max(n for n, _ in seqs),
+                       max_seqlen_k=max(n + c for n, c in seqs))
+    return MixedWorkload(spec=spec, step=step, k_cache0=k0, v_cache0=v0,
+                         scale=1.0 / math.sqrt(d))
 
 
 # ----------------------------------------------------------------------------

@@ -51,6 +51,11 @@ def test_workspace_queries_are_pure(lib):
     assert lib.pkv_paged_decode_workspace_bytes(64, 16, 8192, c) >= a
     p = lib.pkv_paged_prefill_workspace_bytes(16, 16384, 32, c)
     assert p >= 8 * (16384 // 64 + 16)
+    # the mixed-batch call holds the prefill's schedule and a decode plan
+    m = lib.pkv_paged_attention_varlen_workspace_bytes(16, 16384, 32, 8192, c)
+    assert m >= p + lib.pkv_paged_decode_workspace_bytes(16, 32, 8192, c)
+    assert m == lib.pkv_paged_attention_varlen_workspace_bytes(16, 16384, 32, 8192, c)
+    assert lib.pkv_paged_attention_varlen_workspace_bytes(16, 16384, 0, 8192, c) == 0
 
 
 def test_host_checks_return_codes_without_a_gpu(lib):
@@ -88,6 +93,19 @@ def test_host_checks_return_codes_without_a_gpu(lib):
     assert lib.pkv_sample(p, p, p, 1, 10, p, None, None) == -4
     assert lib.pkv_kv_store_paged_prefill_varlen(p, p, p, p, p, p, p, p, 1, 4, 4, 4, 2, None, 0,
                                                  1.0, p, p, 1 << 20, c, None, None) == -4
+    # the mixed-batch call: the prefill's checks, then block tables and the
+    # combined workspace, all before anything is enqueued
+    mixed = lib.pkv_kv_store_paged_attention_varlen
+    assert mixed(None, None, None, None, None, None, None, None, 1, 4, 4, 4, 2, None, 0, 1.0,
+                 None, None, 0, c, None, None) == -1
+    ok = ctypes.c_void_p(16 * 1024)
+    assert mixed(ok, ok, ok, ok, ok, ok, ok, ok, 1, 4, 4, 4, 2, None, 0, 1.0, ok, ok, 1 << 20,
+                 c, None, None) == -1
+    pre = lib.pkv_paged_prefill_workspace_bytes(1, 4, 2, c)
+    assert mixed(ok, ok, ok, ok, ok, ok, ok, ok, 1, 4, 4, 4, 2, ok, 1, 1.0, ok, ok, pre, c,
+                 None, None) == -5
+    assert mixed(ok, ok, ok, ok, ok, ok, ok, ok, 1, 4, 4, 4, 2, ok, 1, 1.0, ok, p, 1 << 20, c,
+                 None, None) == -4
 
 
 def test_layer_cache_pointer_arithmetic(lib):

@@ -77,6 +77,39 @@ def test_prefill_workload_chunks():
     assert all(p == longest[:len(p)] for p in pre)
 
 
+def test_mixed_workload_metadata_and_poison():
+    """A continuous-batching step: decode rows (one new token at ctx-1) first,
+    then prefill chunks; its varlen metadata follows the same slot rules, each
+    decode row's new token lands at its context's last position, and only the
+    cached tokens of the pool hold numbers."""
+    import dataclasses
+    spec = dataclasses.replace(W.MIXED_8B, num_decode=6, num_prefill=3, num_q_heads=4,
+                               num_kv_heads=2, head_dim=8, block_size=16, ctx_lo=1,
+                               ctx_hi=70, new_lo=2, new_hi=40, cached_lo=0, cached_hi=50)
+    w = W.mixed_workload(spec)
+    st, bs = w.step, spec.block_size
+    cu_q, cu_k = st.cu_seqlens_q.tolist(), st.cu_seqlens_k.tolist()
+    tables = [[int(x) for x in row if x >= 0] for row in st.block_tables]
+    seqs = []
+    for j in range(len(cu_q) - 1):
+        lq, lk = cu_q[j + 1] - cu_q[j], cu_k[j + 1] - cu_k[j]
+        assert (lq == 1) == (j < spec.num_decode)
+        assert lk - lq == st.q_start[j]
+        assert len(tables[j]) == oslots.num_blocks(lk, bs)
+        if lq == 1:
+            assert st.slot_mapping[cu_q[j]] == oslots.decode_slot(tables[j], lk, bs)
+        seqs.append((lk - lq, lq, tables[j]))
+    _, cq, ck, sl = oslots.prefill_metadata(seqs, bs)
+    assert cq == cu_q and ck == cu_k and st.slot_mapping.tolist() == sl
+    # every block belongs to one sequence; cached rows hold numbers, the rest NaN
+    flat = sorted(b for t in tables for b in t)
+    assert flat == list(range(w.k_cache0.shape[0]))
+    for t, (cached, _, _) in zip(tables, seqs):
+        for pos in range(len(t) * bs):
+            row = w.k_cache0[t[pos // bs], pos % bs]
+            assert bool(torch.isnan(row).all()) == (pos >= cached)
+
+
 def test_chunk_plan_walkthrough_and_flag():
     # one 600-token prompt with 256 cached: new tokens 344 at budget 200
     assert W.chunk_plan([344], 200, False) == [[(0, 0, 200)], [(0, 200, 144)]]

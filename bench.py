@@ -741,6 +741,16 @@ def profile_case(name: str, calls: int):
         for _ in range(calls):
             pkv.sample(lg, tp, en)
             pkv.sample_philox(lg, tp, 1234, 0)
+    elif name == "mixed-8b":
+        spec = W.MIXED_8B
+        w = W.mixed_workload(spec, device=dev)
+        st = w.step
+        cu_q, cu_k = st.cu_seqlens_q.to(dev), st.cu_seqlens_k.to(dev)
+        bt, sl = st.block_tables.to(dev), st.slot_mapping.to(dev)
+        for _ in range(calls):
+            pkv.kv_store_paged_attention_varlen(st.q, st.k, st.v, w.k_cache0, w.v_cache0, sl,
+                                                cu_q, cu_k, st.max_seqlen_q, st.max_seqlen_k,
+                                                bt, w.scale)
     else:
         raise SystemExit(f"unknown profile case {name!r}")
     torch.cuda.synchronize()
@@ -763,7 +773,7 @@ def main():
     ap.add_argument("--budget", type=float, default=20.0)
     ap.add_argument("--profile", default=None,
                     help="run a small case for ncu instead of the benchmark: decode-0.6b, "
-                         "prefill-8b or sample (calls = --steps)")
+                         "prefill-8b, sample or mixed-8b (calls = --steps)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

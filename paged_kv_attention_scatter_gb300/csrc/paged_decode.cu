@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    allow_dependent_launch();
     wait_for_predecessor();                  // the plan kernel's prefix sums
+    allow_dependent_launch();                // after the wait: see the TMA kernel
     const int units_per_sc = a.Hkv * a.n_hg;
     const int32_t total_sc = a.chunk_prefix[a.B];
     const int64_t units = (int64_t)total_sc * units_per_sc;
@@ -353,11 +353,14 @@ constexpr int kCombineHeads = 4;     // q heads per combine CTA, one warp each
 template <int D>
 __global__ void __launch_bounds__(32 * kCombineHeads) decode_combine_kernel(DecodeArgs a) {
     constexpr int E = D / 32;
-    wait_for_predecessor();                  // the split kernel's partials
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t h = blockIdx.x * kCombineHeads + warp, b = a.b0 + (int32_t)blockIdx.y;
-    if (h >= a.Hq) return;
+    // The plan's prefix is final before this grid launches (the split kernels
+    // allow it only after their own wait for the plan), so it is read ahead
+    // of the wait for the split kernel's partials.
     const int32_t p0 = a.chunk_prefix[b], n = a.chunk_prefix[b + 1] - p0;
+    wait_for_predecessor();                  // the split kernel's partials
+    if (h >= a.Hq) return;
     if (n == 1) return;                                  // written by the split kernel
     if (n == 0 && a.cu_q != nullptr) return;             // not a decode row of a varlen batch
     const int d0 = lane * E;

@@ -128,8 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init_fence();
     }
     __syncthreads();
-    pkv::allow_dependent_launch();
     pkv::wait_for_predecessor();                 // the plan kernel's chunk records
+    // The combine may launch from here on: every CTA has seen the plan done,
+    // so the combine can read the chunk prefix before its own wait.
+    pkv::allow_dependent_launch();
 
     const int units_per_sc = a.Hkv * a.n_hg;
     const int64_t units = (int64_t)a.chunk_prefix[a.B] * units_per_sc;

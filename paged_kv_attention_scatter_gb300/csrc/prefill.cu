@@ -26,39 +26,63 @@ using pkv::PrefillArgs;
 namespace {
 
 constexpr int kBins = 4096;
+constexpr int kPlanThreads = 1024;
+
+// Lengths of the sequences base .. base+kPlanThreads-1 into shared memory, one
+// sequence per thread (one load round trip for the whole group); lq = -1 marks
+// a sequence that gets no tiles (inconsistent lengths, reported when `report`,
+// or a one-query sequence left to the decode kernels).
+__device__ __forceinline__ void load_lengths(const PrefillArgs& a, int32_t base, bool report,
+                                             int32_t* s_lq, int32_t* s_lk) {
+    const int32_t b = base + (int32_t)threadIdx.x;
+    int32_t q0 = 0, lq = -1, lk = 0;
+    if (b < a.B) {
+        if (!pkv::seq_lengths(a, b, q0, lq, lk, report) || (a.skip_single && lq == 1)) {
+            lq = -1;
+        } else if (report && (lq > a.max_sq || lk > a.max_sk)) {
+            pkv::report(a.status, PKV_STATUS_BAD_SEQLENS);
+        }
+    }
+    s_lq[threadIdx.x] = lq;
+    s_lk[threadIdx.x] = lk;
+}
 
 // One CTA: the (sequence, q tile) list ordered by decreasing number of key
-// tiles (a counting sort), so the longest tiles start first.  A warp takes a
-// sequence, its lanes the sequence's q tiles.  The main kernel is launched as
-// a programmatic dependent and waits for this grid before reading the list.
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
+// tiles (a counting sort), so the longest tiles start first.  Each pass reads
+// the lengths of up to 1024 sequences at once, then a warp takes a sequence
+// and its lanes the sequence's q tiles.  The main kernel is launched as a
+// programmatic dependent and waits for this grid before reading the list.
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillArgs a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int32_t hist[kBins];
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t total;
-    for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
+    __shared__ int32_t s_lq[kPlanThreads], s_lk[kPlanThreads];
+    for (int i = threadIdx.x; i < kBins; i += kPlanThreads) hist[i] = 0;
     if (threadIdx.x == 0) total = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    for (int32_t b = w; b < a.B; b += nwarps) {
-        int32_t q0, lq, lk;
-        if (!pkv::seq_lengths(a, b, q0, lq, lk, lane == 0)) continue;
-        if (a.skip_single && lq == 1) continue;      // a decode row, attended elsewhere
-        if (lane == 0 && (lq > a.max_sq || lk > a.max_sk))
-            pkv::report(a.status, PKV_STATUS_BAD_SEQLENS);
-        const int32_t c = lk - lq;
-        const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
-        for (int32_t m = lane; m < nt; m += 32) {
-            const int32_t lim = min(lk, c + (m + 1) * a.tile_m);
-            const int32_t cost = min((lim + a.tile_n - 1) / a.tile_n, kBins - 1);
-            atomicAdd(&hist[kBins - 1 - cost], 1);
+    constexpr int nwarps = kPlanThreads / 32;
+    for (int32_t base = 0; base < a.B; base += kPlanThreads) {
+        load_lengths(a, base, true, s_lq, s_lk);
+        __syncthreads();
+        const int32_t nb = min(kPlanThreads, a.B - base);
+        for (int32_t i = w; i < nb; i += nwarps) {
+            const int32_t lq = s_lq[i], lk = s_lk[i];
+            if (lq < 0) continue;
+            const int32_t c = lk - lq;
+            const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
+            for (int32_t m = lane; m < nt; m += 32) {
+                const int32_t lim = min(lk, c + (m + 1) * a.tile_m);
+                const int32_t cost = min((lim + a.tile_n - 1) / a.tile_n, kBins - 1);
+                atomicAdd(&hist[kBins - 1 - cost], 1);
+            }
+            if (lane == 0) atomicAdd(&total, nt);
         }
-        if (lane == 0) atomicAdd(&total, nt);
+        __syncthreads();
     }
-    __syncthreads();
     // exclusive scan of hist: 4 bins per thread
-    constexpr int per = kBins / 1024;
+    constexpr int per = kBins / kPlanThreads;
     int32_t local[per];
     int32_t sum = 0;
 #pragma unroll
@@ -92,22 +116,26 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillArgs a) {
     }
     __syncthreads();
     bool overflow = false;
-    for (int32_t b = w; b < a.B; b += nwarps) {
-        int32_t q0, lq, lk;
-        if (!pkv::seq_lengths(a, b, q0, lq, lk, false)) continue;
-        if (a.skip_single && lq == 1) continue;
-        const int32_t c = lk - lq;
-        const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
-        for (int32_t m = lane; m < nt; m += 32) {
-            const int32_t lim = min(lk, c + (m + 1) * a.tile_m);
-            const int32_t cost = min((lim + a.tile_n - 1) / a.tile_n, kBins - 1);
-            const int32_t pos = atomicAdd(&hist[kBins - 1 - cost], 1);
-            if (pos < a.max_tiles) a.tiles[pos] = make_int2(b, m);
-            else overflow = true;
+    for (int32_t base = 0; base < a.B; base += kPlanThreads) {
+        load_lengths(a, base, false, s_lq, s_lk);
+        __syncthreads();
+        const int32_t nb = min(kPlanThreads, a.B - base);
+        for (int32_t i = w; i < nb; i += nwarps) {
+            const int32_t lq = s_lq[i], lk = s_lk[i];
+            if (lq < 0) continue;
+            const int32_t c = lk - lq;
+            const int32_t nt = (lq + a.tile_m - 1) / a.tile_m;
+            for (int32_t m = lane; m < nt; m += 32) {
+                const int32_t lim = min(lk, c + (m + 1) * a.tile_m);
+                const int32_t cost = min((lim + a.tile_n - 1) / a.tile_n, kBins - 1);
+                const int32_t pos = atomicAdd(&hist[kBins - 1 - cost], 1);
+                if (pos < a.max_tiles) a.tiles[pos] = make_int2(base + i, m);
+                else overflow = true;
+            }
         }
+        __syncthreads();
     }
     if (overflow) pkv::report(a.status, PKV_STATUS_WORKSPACE_OVERFLOW);
-    __syncthreads();
     if (threadIdx.x == 0) {
         a.sched[0] = min(total, a.max_tiles);
         a.sched[1] = 0;
@@ -402,14 +430,14 @@ int pkv_launch_prefill_plan(PrefillArgs& a, cudaStream_t s, const PrefillPrologu
         if (rc != PKV_OK) return rc;
     }
     if (!chained) {
-        prefill_plan_kernel<<<1, 1024, 0, s>>>(a);
+        prefill_plan_kernel<<<1, kPlanThreads, 0, s>>>(a);
     } else {
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, 1);
-        cfg.blockDim = dim3(1024, 1, 1);
+        cfg.blockDim = dim3(kPlanThreads, 1, 1);
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;

@@ -165,3 +165,34 @@ def test_mixed_batch_in_a_cuda_graph(cuda):
     assert U.status_word(st) == 0
     assert _same(kc1, kc2) and _same(vc1, vc2)
     assert torch.equal(o1, out)
+
+
+def test_mixed_8b_sampled_rows(cuda):
+    """The benchmark's mixed-8b step (256 decode rows and 4 prefill chunks,
+    32/8 heads, 256-slot blocks) in the call bench.py times; the oracle
+    computes sampled rows one by one: 32 decode rows and 8 rows of each chunk."""
+    pkv = U.lib()
+    from paged_kv_attention_scatter_gb300 import workloads as W
+    spec = W.MIXED_8B
+    w = W.mixed_workload(spec, device=cuda)
+    st = w.step
+    kc0, vc0 = w.k_cache0.cpu(), w.v_cache0.cpu()          # before the store
+    status = pkv.new_status(cuda)
+    out = pkv.kv_store_paged_attention_varlen(
+        st.q, st.k, st.v, w.k_cache0, w.v_cache0, st.slot_mapping.to(cuda),
+        st.cu_seqlens_q.to(cuda), st.cu_seqlens_k.to(cuda), st.max_seqlen_q, st.max_seqlen_k,
+        st.block_tables.to(cuda), w.scale, status=status)
+    assert U.status_word(status) == 0
+    cu_q = st.cu_seqlens_q.numpy()
+    rng = np.random.default_rng(5)
+    rows = {int(b): [0] for b in rng.choice(spec.num_decode, size=32, replace=False)}
+    for b in range(spec.num_decode, spec.num_decode + spec.num_prefill):
+        n = int(cu_q[b + 1] - cu_q[b])
+        rows[b] = sorted({0, n - 1} | set(rng.integers(0, n, size=6).tolist()))
+    ref = oatt.paged_prefill_varlen(U.f64(st.q.cpu()), U.f64(st.k.cpu()), U.f64(st.v.cpu()),
+                                    kc0, vc0, cu_q, st.cu_seqlens_k.numpy(),
+                                    st.block_tables.numpy(), w.scale, rows=rows)
+    mask = ~np.isnan(ref[:, 0, 0])
+    assert mask.sum() == 32 + sum(len(r) for b, r in rows.items() if b >= spec.num_decode)
+    err, rel = U.assert_close(U.f64(out)[mask], ref[mask], "mixed-8b sampled rows")
+    print(f"mixed-8b: {mask.sum()} rows, max abs {err:.3g}, rel L2 {rel:.3g}")

@@ -22,12 +22,15 @@
 //
 // Roles (224 threads, one CTA per SM):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
-//              masks (diagonal and partial tiles only), keeps a running row
-//              maximum that is only raised (and O, l rescaled) when the new
-//              maximum exceeds it by more than 2^8 (the row maximum and sum are
-//              taken over independent partial chains), and stores P = exp2(S - m)
-//              as packed bf16 back into the first 64 columns of the same S
-//              buffer; at the end it normalises O.
+//              masks (diagonal and partial tiles only) and stores
+//              P = exp2(S - m) as packed bf16 back into the first 64 columns of
+//              the same S buffer; at the end it normalises O.  m is a running
+//              row maximum: the first tile of an item takes its maximum first,
+//              every later tile computes P against m straight away and is
+//              redone -- maximum taken, m raised and O, l rescaled when it grew
+//              by more than 2^8 -- only if its row sum passed 2^16.  The
+//              exponent argument and the row sum use packed f32x2 instructions
+//              (one per column pair).
 //   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
 //              three-stage ring.  A K stage is refilled as soon as its Q K^T
 //              is done, a V stage once its P V is done.
@@ -72,6 +75,10 @@ constexpr int kItemReaders = 6;          // Q K^T issuer, P V issuer, 4 softmax 
 constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
+// A tile computed against the running maximum is redone (maximum taken, O and
+// l rescaled) when its row sum of P passes 2^16, i.e. when some exponent may
+// exceed 9; P stays below 2^16 otherwise, far inside the fp32 / bf16 range.
+constexpr float kSumTrigger = 65536.0f;
 
 template <int D>
 struct __align__(1024) TcSmem {
@@ -118,6 +125,28 @@ __device__ __forceinline__ Item item_at(const PrefillArgs& a, int64_t it) {
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed pairs of fp32 (one 64-bit register pair): fma.rn.f32x2 and add.f32x2
+// do two lanes' worth of work per instruction, each lane rounded as the scalar
+// instruction would be.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 
@@ -413,60 +442,88 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     lim = i + 1;
                     masked = true;
                 }
-                // eight independent partial maxima (no 128-long dependency
-                // chain), two new columns per three-input max
                 if (masked) {
 #pragma unroll
                     for (int col = 0; col < kBN; ++col) sv[col] = col < lim ? sv[col] : -INFINITY;
                 }
-                float mxp[8];
+                // P = exp2(S*scale - m) into the first 64 columns of the S
+                // buffer, with the row sum in two packed pairs of chains (the
+                // exponent and the sum take one f32x2 instruction per column
+                // pair).
+                float ls[4];
+                auto exp_pass = [&](float neg_m) {
+                    const uint64_t scale2 = pk2(a.scale_log2, a.scale_log2);
+                    const uint64_t neg_m2 = pk2(neg_m, neg_m);
+                    uint64_t l2[2] = {pk2(0.f, 0.f), pk2(0.f, 0.f)};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mxp[e] = fmaxf(sv[e], sv[8 + e]);
+                    for (int half = 0; half < 2; ++half) {
+                        float pw[32];                           // packed bf16 pairs
 #pragma unroll
-                for (int col = 16; col < kBN; col += 16)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mxp[e] = max3(mxp[e], sv[col + e], sv[col + 8 + e]);
-                float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-                mx *= a.scale_log2;                         // scale > 0 keeps the order
-                const bool raise = mx > m_run + kRescaleThreshold;
-                float alpha = 1.f;
-                if (raise) {
-                    alpha = (m_run == -INFINITY) ? 0.f : pkv::fast_exp2(m_run - mx);
-                    m_run = mx;
-                    l_run *= alpha;
-                }
-                if (j > 0 && __any_sync(0xffffffffu, raise)) {
-                    // O may only be rescaled once the previous P V has finished
-                    const uint32_t tp = t - 1;
-                    if (!(ok = warp_wait(&s.pv_done[tp % kStages], (tp / kStages) & 1,
-                                         &s.abort_flag)))
-                        break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        float ov[32];
-                        tmem_ld32(lane_base + kColO + cc * 32, ov);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-                        tmem_st32(lane_base + kColO + cc * 32, ov);
+                        for (int e = 0; e < 32; ++e) {
+                            const int col = half * 64 + 2 * e;
+                            float x0, x1;
+                            up2(fma2(pk2(sv[col], sv[col + 1]), scale2, neg_m2), x0, x1);
+                            const float p0 = pkv::fast_exp2(x0);
+                            const float p1 = pkv::fast_exp2(x1);
+                            l2[e & 1] = add2(l2[e & 1], pk2(p0, p1));
+                            pw[e] = __uint_as_float(pkv::pack_bf16(p0, p1));
+                        }
+                        tmem_st32(s_col + half * 32, pw);       // P aliases S columns 0..63
                     }
+                    up2(l2[0], ls[0], ls[1]);
+                    up2(l2[1], ls[2], ls[3]);
+                };
+                // After the first tile, P is computed straight away against the
+                // running maximum; only when some row's sum passes kSumTrigger
+                // (rare: the maximum grew by more than 2^9) is the tile's
+                // maximum taken and P recomputed.  The first tile of an item
+                // takes the maximum first.
+                bool redo = j == 0;
+                if (!redo) {
+                    exp_pass(-m_run);
+                    const float lt = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    redo = __any_sync(0xffffffffu, !(lt <= kSumTrigger));
+                    if (redo) tmem_wait_st();                   // before P is stored again
                 }
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};       // independent partial sums
+                if (redo) {
+                    // eight independent partial maxima (no 128-long dependency
+                    // chain), two new columns per three-input max
+                    float mxp[8];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float pw[32];                               // packed bf16 pairs
+                    for (int e = 0; e < 8; ++e) mxp[e] = fmaxf(sv[e], sv[8 + e]);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int col = half * 64 + 2 * e;
-                        const float p0 = pkv::fast_exp2(fmaf(sv[col], a.scale_log2, neg_m));
-                        const float p1 = pkv::fast_exp2(fmaf(sv[col + 1], a.scale_log2, neg_m));
-                        ls[e & 3] += p0 + p1;
-                        pw[e] = __uint_as_float(pkv::pack_bf16(p0, p1));
+                    for (int col = 16; col < kBN; col += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            mxp[e] = max3(mxp[e], sv[col + e], sv[col + 8 + e]);
+                    float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                     fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+                    mx *= a.scale_log2;                     // scale > 0 keeps the order
+                    const bool raise = mx > m_run + kRescaleThreshold;
+                    float alpha = 1.f;
+                    if (raise) {
+                        alpha = (m_run == -INFINITY) ? 0.f : pkv::fast_exp2(m_run - mx);
+                        m_run = mx;
+                        l_run *= alpha;
                     }
-                    tmem_st32(s_col + half * 32, pw);           // P aliases S columns 0..63
+                    if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                        // O may only be rescaled once the previous P V has finished
+                        const uint32_t tp = t - 1;
+                        if (!(ok = warp_wait(&s.pv_done[tp % kStages], (tp / kStages) & 1,
+                                             &s.abort_flag)))
+                            break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            float ov[32];
+                            tmem_ld32(lane_base + kColO + cc * 32, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+                            tmem_st32(lane_base + kColO + cc * 32, ov);
+                        }
+                    }
+                    exp_pass((m_run == -INFINITY) ? 0.f : -m_run);
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 tmem_wait_st();

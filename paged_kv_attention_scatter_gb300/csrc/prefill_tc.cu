@@ -20,7 +20,7 @@
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
 // shared memory because unused cache slots may hold NaN.
 //
-// Roles (224 threads, one CTA per SM):
+// Roles (256 threads, one CTA per SM):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks (diagonal and partial tiles only) and stores
 //              P = exp2(S - m) as packed bf16 back into the first 64 columns of
@@ -31,9 +31,11 @@
 //              by more than 2^8 -- only if its row sum passed 2^16.  The
 //              exponent argument and the row sum use packed f32x2 instructions
 //              (one per column pair).
-//   warp 4     TMA producer (one thread): Q once per item, K/V tiles into a
-//              three-stage ring.  A K stage is refilled as soon as its Q K^T
-//              is done, a V stage once its P V is done.
+//   warp 4     TMA producer (one thread): Q once per item, K tiles into a
+//              three-stage ring, a stage refilled as soon as its Q K^T is done.
+//   warp 7     TMA producer of the V tiles (one thread, three stages), a stage
+//              refilled once its P V is done; on its own thread so that wait
+//              never holds back a K tile.
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for
@@ -68,10 +70,10 @@ constexpr int kBN = 128;                 // keys per tile
 // head_dim D is 128 or 64: a tile is D/64 column blocks of 64 bf16 (one
 // 128-byte swizzle atom wide), each 128 rows x 128 B
 constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
-constexpr int kItemReaders = 6;          // Q K^T issuer, P V issuer, 4 softmax warps
+constexpr int kItemReaders = 7;          // V producer, Q K^T and P V issuers, 4 softmax warps
 constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
@@ -184,6 +186,64 @@ __device__ __forceinline__ void give_up(Smem& s, uint32_t* status) {
     pkv::report(status, PKV_STATUS_WAIT_TIMEOUT);
 }
 
+// Where tile j of item x comes from: the chunk's own rows (map k/v, one box at
+// `row`), or the cache through the block table (one box at `row`, or with
+// kBoxed one box per block at rows[]; keys past the prefix or the pool read
+// zeros).  Returns whether it is a cached tile; sets `bad` on a block id
+// outside the pool.
+template <bool kBoxed>
+__device__ __forceinline__ bool tile_source(const PrefillArgs& a, const Item& x, int32_t j,
+                                            int32_t& row, int32_t* rows, bool& bad) {
+    const int32_t oob_row = a.NB * a.bs;   // past the pool: TMA fills zeros
+    row = oob_row;
+    if (j >= x.n_cached) {
+        row = x.q0 + (j - x.n_cached) * kBN;
+        return false;
+    }
+    const int32_t key0 = j * kBN;
+    if (!kBoxed) {
+        const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
+        if ((unsigned)blk < (unsigned)a.NB)
+            row = blk * a.bs + key0 % a.bs;
+        else
+            bad = true;
+    } else {
+#pragma unroll
+        for (int u = 0; u < kMaxBoxes; ++u) {
+            rows[u] = oob_row;
+            const int32_t key = key0 + u * a.bs;
+            if (key < key0 + kBN && key < x.c) {
+                const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
+                if ((unsigned)blk < (unsigned)a.NB)
+                    rows[u] = blk * a.bs + key % a.bs;
+                else
+                    bad = true;
+            }
+        }
+    }
+    return true;
+}
+
+// One tile (K or V) into a stage: one box per 64-column block, or with kBoxed
+// and a cached tile one box per block of the pool, stacked.
+template <int D, bool kBoxed>
+__device__ __forceinline__ void load_tile(unsigned char* dst, const CUtensorMap* map,
+                                          uint64_t* bar, int kvh, bool cached, int32_t row,
+                                          const int32_t* rows, int32_t bs) {
+    constexpr int kBlocks = D / 64;
+    if (!(kBoxed && cached)) {
+        for (int hf = 0; hf < kBlocks; ++hf)
+            tma_load_3d(dst + hf * kHalf, map, bar, hf * 64, kvh, row);
+    } else {
+#pragma unroll
+        for (int u = 0; u < kMaxBoxes; ++u)
+            if (u * bs < kBN)
+#pragma unroll
+                for (int hf = 0; hf < kBlocks; ++hf)
+                    tma_load_3d(dst + hf * kHalf + u * bs * 128, map, bar, hf * 64, kvh, rows[u]);
+    }
+}
+
 // kBoxed: the pool's blocks hold fewer than 128 keys, so a cached tile is
 // gathered from 128/bs boxes (a separate instantiation keeps the common
 // one-box producer loop free of that code).
@@ -238,8 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             }
             uint32_t T = 0, I = 0;
             bool ok = true, bad_block = false;
-            const int32_t oob_row = a.NB * a.bs;   // past the pool: TMA fills zeros
-            const int cache_box = kBoxed ? a.bs : kBN;
             for (; ok; ++I) {
                 // the next item of the cost-sorted list, taken dynamically so
                 // the CTAs finish together; the other roles read it from the ring
@@ -263,72 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     const uint32_t use = T / kStages;
                     if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_flag)))
                         break;
-                    // a tile is one box of 128 rows, or (cached tiles of a pool with
-                    // blocks below 128 keys) one box per block, stacked
-                    const CUtensorMap* mk;
-                    const CUtensorMap* mv;
-                    int32_t row = oob_row;
-                    int32_t rows[kMaxBoxes];
-                    const bool boxed = kBoxed && j < x.n_cached;
-                    if (j < x.n_cached) {
-                        const int32_t key0 = j * kBN;
-                        if (!boxed) {
-                            const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
-                            if ((unsigned)blk < (unsigned)a.NB)
-                                row = blk * a.bs + key0 % a.bs;
-                            else
-                                bad_block = true;
-                        } else {
-#pragma unroll
-                            for (int u = 0; u < kMaxBoxes; ++u) {
-                                rows[u] = oob_row;
-                                const int32_t key = key0 + u * cache_box;
-                                if (key < key0 + kBN && key < x.c) {   // past the prefix: zeros
-                                    const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
-                                    if ((unsigned)blk < (unsigned)a.NB)
-                                        rows[u] = blk * a.bs + key % a.bs;
-                                    else
-                                        bad_block = true;
-                                }
-                            }
-                        }
-                        mk = &maps.kc;
-                        mv = &maps.vc;
-                    } else {
-                        row = x.q0 + (j - x.n_cached) * kBN;
-                        mk = &maps.k;
-                        mv = &maps.v;
-                    }
+                    int32_t row, rows[kMaxBoxes];
+                    const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
                     mbar_expect_tx(&s.k_full[st], kTile);
-                    if (!boxed) {
-                        for (int hf = 0; hf < kBlocks; ++hf)
-                            tma_load_3d(s.k[st] + hf * kHalf, mk, &s.k_full[st], hf * 64, kvh, row);
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < kMaxBoxes; ++u)
-                            if (u * cache_box < kBN)
-#pragma unroll
-                                for (int hf = 0; hf < kBlocks; ++hf)
-                                    tma_load_3d(s.k[st] + hf * kHalf + u * cache_box * 128, mk,
-                                                &s.k_full[st], hf * 64, kvh, rows[u]);
-                    }
-                    if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag))) {
-                        mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
-                        break;
-                    }
-                    mbar_expect_tx(&s.v_full[st], kTile);
-                    if (!boxed) {
-                        for (int hf = 0; hf < kBlocks; ++hf)
-                            tma_load_3d(s.v[st] + hf * kHalf, mv, &s.v_full[st], hf * 64, kvh, row);
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < kMaxBoxes; ++u)
-                            if (u * cache_box < kBN)
-#pragma unroll
-                                for (int hf = 0; hf < kBlocks; ++hf)
-                                    tma_load_3d(s.v[st] + hf * kHalf + u * cache_box * 128, mv,
-                                                &s.v_full[st], hf * 64, kvh, rows[u]);
-                    }
+                    load_tile<D, kBoxed>(s.k[st], cached ? &maps.kc : &maps.k, &s.k_full[st], kvh,
+                                         cached, row, rows, a.bs);
                 }
             }
             if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
@@ -338,6 +335,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 for (int back = 1; back <= kStages && (int)T - back >= 0; ++back) {
                     const uint32_t t = T - back;
                     mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
+                }
+            }
+        }
+    } else if (warp == 7) {
+        // ------------------------------------------------------------ V producer
+        // V tiles on their own thread: a V stage waits for its P V, and in
+        // the producer's loop that wait held back the next K tile
+        if (lane == 0) {
+            uint32_t T = 0, I = 0;
+            bool ok = true, bad_block = false;
+            for (; ok; ++I) {
+                int32_t it = -1;
+                if (!(ok = next_item(s, I, it))) break;
+                if (it < 0) break;
+                const Item x = item_at(a, it);
+                const int32_t kvh = x.h / a.G;
+                for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
+                    const int st = T % kStages;
+                    const uint32_t use = T / kStages;
+                    if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag)))
+                        break;
+                    int32_t row, rows[kMaxBoxes];
+                    const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
+                    mbar_expect_tx(&s.v_full[st], kTile);
+                    load_tile<D, kBoxed>(s.v[st], cached ? &maps.vc : &maps.v, &s.v_full[st], kvh,
+                                         cached, row, rows, a.bs);
+                }
+            }
+            if (!ok) {
+                give_up(s, a.status);
+                for (int back = 1; back <= kStages && (int)T - back >= 0; ++back) {
+                    const uint32_t t = T - back;
                     mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
                 }
             }

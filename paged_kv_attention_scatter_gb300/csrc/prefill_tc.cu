@@ -70,10 +70,16 @@ constexpr int kBN = 128;                 // keys per tile
 // head_dim D is 128 or 64: a tile is D/64 column blocks of 64 bf16 (one
 // 128-byte swizzle atom wide), each 128 rows x 128 B
 constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;            // 224 (no V producer warp) with kBoxed
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
 constexpr int kItemReaders = 7;          // V producer, Q K^T and P V issuers, 4 softmax warps
+// With kBoxed the K producer also loads V (a second thread gathering the same
+// boxes measured 10-14% slower), so the V producer warp is not launched.
+template <bool kBoxed>
+constexpr int threads_for() { return kBoxed ? kThreads - 32 : kThreads; }
+template <bool kBoxed>
+constexpr int item_readers_for() { return kBoxed ? kItemReaders - 1 : kItemReaders; }
 constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         mbar_init(&s.o_free, 128);
         for (int q = 0; q < kItemRing; ++q) {
             mbar_init(&s.item_full[q], 1);
-            mbar_init(&s.item_empty[q], kItemReaders);
+            mbar_init(&s.item_empty[q], item_readers_for<kBoxed>());
         }
         mbar_init(&s.mma_done, 2);
         mbar_init_fence();
@@ -326,6 +332,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     mbar_expect_tx(&s.k_full[st], kTile);
                     load_tile<D, kBoxed>(s.k[st], cached ? &maps.kc : &maps.k, &s.k_full[st], kvh,
                                          cached, row, rows, a.bs);
+                    if constexpr (kBoxed) {
+                        if (use > 0 &&
+                            !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag))) {
+                            mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
+                            break;
+                        }
+                        mbar_expect_tx(&s.v_full[st], kTile);
+                        load_tile<D, kBoxed>(s.v[st], cached ? &maps.vc : &maps.v, &s.v_full[st],
+                                             kvh, cached, row, rows, a.bs);
+                    }
                 }
             }
             if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
@@ -335,10 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 for (int back = 1; back <= kStages && (int)T - back >= 0; ++back) {
                     const uint32_t t = T - back;
                     mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
+                    if (kBoxed) mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
                 }
             }
         }
-    } else if (warp == 7) {
+    } else if (!kBoxed && warp == 7) {
         // ------------------------------------------------------------ V producer
         // V tiles on their own thread: a V stage waits for its P V, and in
         // the producer's loop that wait held back the next K tile
@@ -640,7 +657,7 @@ int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(boxed ? threads_for<true>() : threads_for<false>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;

@@ -158,6 +158,13 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return r;
 }
 
+// 32 bytes to global memory in one instruction (address 32-byte aligned).
+__device__ __forceinline__ void st_global_32b(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // All 32 lanes wait on the same barrier; the result is made warp-uniform so
 // the warp-wide TMEM instructions that follow never see a diverged warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const int* abort_flag) {
@@ -598,20 +605,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             __nv_bfloat16* orow = a.out + ((int64_t)(x.q0 + x.m * kBM + i) * a.Hq + x.h) * D;
+            // a row is 32-byte aligned when `out` is (rows are D*2 bytes):
+            // then 32 bytes per store, a whole sector each (each store of a
+            // warp lands in 32 different rows, so the store count sets the
+            // cost)
+            const bool wide = ((uintptr_t)a.out & 31) == 0;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 float ov[32];
                 tmem_ld32(lane_base + kColO + cc * 32, ov);
                 tmem_wait_ld();
                 if (i < x.rows) {
+                    if (wide) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 pk;
-                        pk.x = pkv::pack_bf16(ov[q4 * 8 + 0] * inv, ov[q4 * 8 + 1] * inv);
-                        pk.y = pkv::pack_bf16(ov[q4 * 8 + 2] * inv, ov[q4 * 8 + 3] * inv);
-                        pk.z = pkv::pack_bf16(ov[q4 * 8 + 4] * inv, ov[q4 * 8 + 5] * inv);
-                        pk.w = pkv::pack_bf16(ov[q4 * 8 + 6] * inv, ov[q4 * 8 + 7] * inv);
-                        *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pk;
+                        for (int q2 = 0; q2 < 2; ++q2) {
+                            uint32_t w8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                w8[e] = pkv::pack_bf16(ov[q2 * 16 + 2 * e] * inv,
+                                                       ov[q2 * 16 + 2 * e + 1] * inv);
+                            st_global_32b(orow + cc * 32 + q2 * 16, w8);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 pk;
+                            pk.x = pkv::pack_bf16(ov[q4 * 8 + 0] * inv, ov[q4 * 8 + 1] * inv);
+                            pk.y = pkv::pack_bf16(ov[q4 * 8 + 2] * inv, ov[q4 * 8 + 3] * inv);
+                            pk.z = pkv::pack_bf16(ov[q4 * 8 + 4] * inv, ov[q4 * 8 + 5] * inv);
+                            pk.w = pkv::pack_bf16(ov[q4 * 8 + 6] * inv, ov[q4 * 8 + 7] * inv);
+                            *reinterpret_cast<uint4*>(orow + cc * 32 + q4 * 8) = pk;
+                        }
                     }
                 }
             }

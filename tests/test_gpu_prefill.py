@@ -86,6 +86,25 @@ def test_ragged_cached_prefixes(cuda, hq, hkv, d, bs):
     _check_case(pkv, cuda, c, 1.0 / math.sqrt(d))
 
 
+@pytest.mark.parametrize("d,bs", [(128, 256), (64, 256), (128, 16)])
+def test_output_only_16_byte_aligned(cuda, d, bs):
+    """An output buffer at a 16-byte (not 32-byte) boundary takes the 16-byte
+    store path of the epilogue; its rows equal those of an aligned output."""
+    pkv = U.lib()
+    lens, cached = [200, 1, 129], [0, 48, 2 * bs]
+    c = make_case(123 + d + bs, lens, cached, 8, 2, d, bs)
+    args = (c["q"].to(cuda), c["k"].to(cuda), c["v"].to(cuda), c["kc"].to(cuda),
+            c["vc"].to(cuda), c["cu_q"].to(cuda), c["cu_k"].to(cuda), c["max_sq"], c["max_sk"],
+            c["bt"].to(cuda), 1.0 / math.sqrt(d))
+    aligned = pkv.paged_prefill_varlen(*args)
+    buf = torch.zeros(c["q"].numel() + 8, dtype=torch.bfloat16, device=cuda)
+    out = buf[8:].view(c["q"].shape)
+    assert out.data_ptr() % 32 == 16
+    pkv.paged_prefill_varlen(*args, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, aligned)
+
+
 def test_long_single_sequence_no_cache(cuda):
     pkv = U.lib()
     c = make_case(5, [1000], [0], 8, 2, 128, 256)

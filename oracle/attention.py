@@ -10,7 +10,7 @@ Layouts ([UML] §3.2 "Attention运算"; [LIFE] §2.2.3):
   cu_seqlens_q/k    (batch+1,) prefix sums of per-sequence lengths
   context_lens      (batch,) cached keys per sequence (decode)
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * grouped-query attention maps q head h to kv head h // (Hq // Hkv);
   * a query that is row i of a sequence with Lq queries and Lk keys sits at
     absolute position Lk - Lq + i and sees keys j <= that position (the only

@@ -7,7 +7,7 @@ Gumbel-max draw; [LIFE] §4: the sampler runs on each sequence's last-position
 logits and returns one token id per sequence.  The noise is passed in: E is a
 (B, V) array of Exp(1) draws.
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
   * "Gumbel-max" is the exponential race argmax_i p_i / E_i, E_i ~ Exp(1),
     which equals argmax_i (x_i - ln E_i) because softmax is monotone in x;
   * E is clamped below at 1e-10 before it is used;

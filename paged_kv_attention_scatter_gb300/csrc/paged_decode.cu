@@ -434,18 +434,21 @@ cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, cud
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Keys per work unit: a multiple of 64 (4 warps x 16), chosen from the sizes
-// alone so the workspace query and the call agree.  Larger chunks cut the
-// partial-result traffic; smaller ones give the persistent grid more units.
+// Keys per work unit: the multiple of 64 nearest to the length that gives
+// about 16 units per SM (of 152) for a typical context of half the stated
+// maximum, within 64..1024; chosen from the sizes alone so the workspace
+// query and the call agree.  Longer units cut the partial results and the
+// per-unit merges, shorter ones keep the persistent grid's last round short.
+// (Measured on decode-0.6b: powers of two only, 256-key chunks, 6188 GB/s;
+// 320: 6287; 384: 6241; 448: 6357; 512: 5969.  The long workloads keep 1024.)
 int32_t choose_chunk_keys(int32_t batch, int32_t units_per_seq_chunk, int32_t max_ctx) {
-    const int64_t want_units = 8LL * 152 * 3;            // ~8 units per resident CTA
-    int32_t chunk = 1024;
-    while (chunk > 64) {
-        const int64_t per_seq = ((int64_t)max_ctx / 2 + chunk - 1) / chunk;
-        if ((int64_t)batch * units_per_seq_chunk * per_seq >= want_units) break;
-        chunk >>= 1;
-    }
-    return chunk;
+    const double typical = (double)max_ctx / 2.0;
+    const double want_units = 16.0 * 152;
+    const double keys = typical * (double)batch * (double)units_per_seq_chunk / want_units;
+    int64_t chunk = (int64_t)(keys / 64.0 + 0.5) * 64;
+    if (chunk < 64) chunk = 64;
+    if (chunk > 1024) chunk = 1024;
+    return (int32_t)chunk;
 }
 
 struct DecodeLayout {

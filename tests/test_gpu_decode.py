@@ -157,7 +157,7 @@ def test_workspace_too_small_is_rejected(cuda):
 def test_stated_maximum_context_sets_the_chunking(cuda, max_ctx_scale):
     """The chunk size comes from the stated maximum context alone: the exact
     maximum gives 64-key chunks (up to 15 per sequence), a 64x larger one
-    512-key chunks.  Both chunkings must match the oracle."""
+    1024-key chunks.  Both chunkings must match the oracle."""
     pkv = U.lib()
     spec = W.DecodeSpec("merge", seed=77, batch=24, num_q_heads=8, num_kv_heads=4, head_dim=128,
                         block_size=64, ctx_lo=1, ctx_hi=900)

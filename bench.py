@@ -40,8 +40,8 @@ LAYERS_0P6B = 28                   # decoder layers of a Qwen3-0.6B-shaped model
 # its split and combine launches, from one ncu capture (profiles/
 # decode_tma_kernel_decode-0.6b.md).  Valid only for the decode sources it was
 # taken on: the digest below must match, otherwise the traffic is reported null.
-DECODE_0P6B_TRAFFIC = {"bytes": 585769728,
-                       "sources_sha256": "f5ec06216298da30c1ba32822c0651666d0e78d643c6e91f239bf34cafa698fd"}
+DECODE_0P6B_TRAFFIC = {"bytes": 582375168,
+                       "sources_sha256": "4f3671be8474468ac0fcfe30a52d3b3b4518c9ca6ecf37f3d0b5debab6d14c9e"}
 
 DECODE_SOURCES = ["paged_decode.cu", "paged_decode_tma.cu", "decode_common.cuh", "common.cuh",
                   "tc_utils.cuh", "tma_host.cuh"]

@@ -20,11 +20,13 @@
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
 // shared memory because unused cache slots may hold NaN.
 //
-// Roles (256 threads, one CTA per SM):
+// Roles (256 threads, one CTA per SM; 224 without warp 7 when cached tiles
+// are gathered per block):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks (diagonal and partial tiles only) and stores
 //              P = exp2(S - m) as packed bf16 back into the first 64 columns of
-//              the same S buffer; at the end it normalises O.  m is a running
+//              the same S buffer; at the end it normalises O and writes it out
+//              (32-byte stores when the output allows).  m is a running
 //              row maximum: the first tile of an item takes its maximum first,
 //              every later tile computes P against m straight away and is
 //              redone -- maximum taken, m raised and O, l rescaled when it grew
@@ -35,7 +37,8 @@
 //              three-stage ring, a stage refilled as soon as its Q K^T is done.
 //   warp 7     TMA producer of the V tiles (one thread, three stages), a stage
 //              refilled once its P V is done; on its own thread so that wait
-//              never holds back a K tile.
+//              never holds back a K tile.  With per-block boxes warp 4 loads V
+//              too (a second thread walking the same block table was slower).
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for

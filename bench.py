@@ -807,7 +807,7 @@ def main():
                              "kind": "oracle",
                              "sample": f"{r['seqs']} whole sequences (all 16 q heads) of "
                                        "decode-0.6b, one per step, float64 NumPy, "
-                                       "single-threaded BLAS, stopped after 120 s"},
+                                       "single-threaded BLAS, at most 120 s"},
             "e2e": {"value": round(r["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}))
         return

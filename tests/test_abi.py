@@ -58,6 +58,21 @@ def test_workspace_queries_are_pure(lib):
     assert lib.pkv_paged_attention_varlen_workspace_bytes(16, 16384, 0, 8192, c) == 0
 
 
+def test_decode_workspace_follows_the_chunk_choice(lib):
+    """decode-0.6b (64 sequences, 16/8 heads, D=128, max context 4096): 448-key
+    chunks (the multiple of 64 nearest ~16 units per SM), so 10 chunk slots per
+    sequence; the workspace is the chunk prefix, the records, the (max, sum)
+    pairs and the fp32 partial outputs, each 256-byte aligned."""
+    from paged_kv_attention_scatter_gb300._binding import CacheDesc
+    cap = 64 * -(-4096 // 448)
+    align = lambda x: (x + 255) // 256 * 256
+    off_info = align(4 * 65)
+    off_ml = align(off_info + 16 * cap)
+    off_o = align(off_ml + 8 * cap * 16)
+    total = align(off_o + 4 * cap * 16 * 128)
+    assert lib.pkv_paged_decode_workspace_bytes(64, 16, 4096, CacheDesc(572, 256, 8, 128)) == total
+
+
 def test_host_checks_return_codes_without_a_gpu(lib):
     from paged_kv_attention_scatter_gb300._binding import CacheDesc
     c = CacheDesc(8, 4, 1, 64)

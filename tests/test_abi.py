@@ -136,3 +136,24 @@ def test_layer_cache_pointer_arithmetic(lib):
     assert vp.value == base + (4 + 3) * layer_bytes
     assert lib.pkv_layer_cache(base, 4, 4, c, ctypes.byref(kp), ctypes.byref(vp)) == -2
     assert lib.pkv_layer_cache(None, 4, 0, c, ctypes.byref(kp), ctypes.byref(vp)) == -1
+
+
+def test_mixed_batch_binding_checks_before_the_library():
+    """The Python binding of the mixed-batch call rejects a slot list of the
+    wrong length and a missing block table before touching the library."""
+    import pytest
+    import torch
+    from paged_kv_attention_scatter_gb300 import _binding
+    q = torch.zeros(5, 2, 64, dtype=torch.bfloat16)
+    k = torch.zeros(5, 1, 64, dtype=torch.bfloat16)
+    cache = torch.zeros(4, 16, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 1, 5], dtype=torch.int32)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="one slot per query token"):
+        _binding.kv_store_paged_attention_varlen(q, k, k, cache, cache,
+                                                 torch.zeros(4, dtype=torch.int32), cu, cu,
+                                                 4, 4, bt, 0.125)
+    with pytest.raises(ValueError, match="block_tables is required"):
+        _binding.kv_store_paged_attention_varlen(q, k, k, cache, cache,
+                                                 torch.zeros(5, dtype=torch.int32), cu, cu,
+                                                 4, 4, None, 0.125)

@@ -138,7 +138,7 @@ def test_layer_cache_pointer_arithmetic(lib):
     assert lib.pkv_layer_cache(None, 4, 0, c, ctypes.byref(kp), ctypes.byref(vp)) == -1
 
 
-def test_mixed_batch_binding_checks_before_the_library():
+def test_mixed_batch_binding_checks_before_the_library(lib):
     """The Python binding of the mixed-batch call rejects a slot list of the
     wrong length and a missing block table before touching the library."""
     import pytest

@@ -41,11 +41,11 @@ Functions and their pins (all pins are tests under ``tests/`` marked not-gpu):
       lowest-index tie rule.
 
   sampler.philox4x32_10 / philox_words / philox_exp_noise / sample_philox
-      the counter-based noise of the in-kernel-noise sampler.  Parity
-      unpinned for the generator itself (no published known-answer vector is
-      used); checked by inverting its round, by output statistics, and by the
-      Gumbel-max law of the draws it feeds.
+      the counter-based noise of the in-kernel-noise sampler: the generator
+      is pinned to the published Philox4x32-10 known-answer vectors (Random123,
+      Salmon et al., SC 2011); the stream built on it is checked by inverting
+      its round, by output statistics, and by the Gumbel-max law of its draws.
 
-Every other function is pinned.
+Every function is pinned.
 """
 from . import attention, kv_store, sampler, slots  # noqa: F401

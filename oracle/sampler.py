@@ -18,10 +18,11 @@ Readings where the pages are silent:
 In-kernel noise (the library's second sampler entry point) uses the
 counter-based generator Philox4x32-10 of Salmon, Moraes, Dror and Shaw,
 "Parallel random numbers: as easy as 1, 2, 3" (SC 2011), restated below from
-that definition.  `philox4x32_10` is "parity unpinned": no published
-known-answer vector is used; it is checked only by statistics of its output,
-by inverting its round function, and through the Gumbel-max law of the draws
-it feeds.
+that definition.  `philox4x32_10` is pinned to the published known-answer
+vectors of that generator (the known-answer file of the authors' Random123
+library, stored under tests/golden/); the stream built on it is further checked
+by inverting its round function, by statistics of its output, and through the
+Gumbel-max law of the draws it feeds.
 """
 from __future__ import annotations
 

@@ -304,3 +304,27 @@ def check_temperature_matters(sample_fn):
     E = np.array([[1.0, 0.3], [1.0, 0.3]])
     ids, _ = sample_fn(logits, np.array([0.1, 10.0]), E)
     assert ids.tolist() == [0, 1]
+
+
+# ----------------------------------------------------------------------------
+# counter-based generator pin
+# ----------------------------------------------------------------------------
+def philox_kat_cases():
+    """The known-answer cases of tests/golden/philox4x32_10_kat.json as
+    (counter words, key words, output words) integer tuples."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "philox4x32_10_kat.json")
+    gold = json.load(open(path))
+    assert gold["rounds"] == 10
+    return [(tuple(int(x, 16) for x in c["counter"]), tuple(int(x, 16) for x in c["key"]),
+             tuple(int(x, 16) for x in c["output"])) for c in gold["cases"]]
+
+
+def check_philox_kat(block_fn):
+    """block_fn(counters (N, 4), key (k0, k1)) -> (N, 4) words must reproduce
+    the published Philox4x32-10 known-answer vectors word for word."""
+    for ctr, key, want in philox_kat_cases():
+        got = block_fn(np.array([ctr], dtype=np.uint64), key)
+        assert [int(x) for x in np.asarray(got)[0]] == list(want), (ctr, key)

@@ -61,3 +61,33 @@ def test_bad_temperature_rows(cuda):
                             status=st).cpu().tolist()
     assert ids[1:] == [0, 0]
     assert U.status_word(st) == pkv.STATUS["BAD_TEMPERATURE"]
+
+
+@pytest.mark.parametrize("vocab", [16, 13])
+@pytest.mark.parametrize("seed,offset", [(7, 0), ((1 << 37) + 5, (1 << 35) + 2)])
+def test_each_rows_noise_order_follows_the_oracle_words(cuda, vocab, seed, offset):
+    """The whole noise of small rows, not only its largest entry: with equal
+    logits the draw picks the entry with the largest U; masking each winner and
+    drawing again V times gives the kernel's complete order of the row's U
+    values, which must be the order of the oracle's Philox words (w >> 8).  A
+    word taken from the wrong counter, lane or key shows as an out-of-order
+    pair.  Entries whose float64 keys lie within 1e-5 of each other may come
+    in either order (the kernel decides in float32)."""
+    pkv = U.lib()
+    B = 64
+    logits = torch.zeros((B, vocab), device=cuda)
+    temps = torch.ones(B, device=cuda)
+    rows = torch.arange(B, device=cuda)
+    order = np.zeros((B, vocab), dtype=np.int64)
+    for k in range(vocab):
+        ids = pkv.sample_philox(logits, temps, seed, offset)
+        order[:, k] = ids.cpu().numpy()
+        logits[rows, ids.long()] = -1.0e4            # masked: its key stays below -9000
+    assert all(sorted(order[r].tolist()) == list(range(vocab)) for r in range(B))
+    w = osm.philox_words(np.arange(B * vocab), seed, offset).reshape(B, vocab) >> np.uint64(8)
+    u = (w.astype(np.float64) + 1.0) * 2.0 ** -24
+    key = -np.log(np.maximum(-np.log(u), osm.NOISE_FLOOR))        # logits 0, T 1
+    in_order = np.take_along_axis(key, order, axis=1)
+    assert np.all(in_order[:, :-1] >= in_order[:, 1:] - 1e-5)
+    exact = np.argsort(-w.astype(np.int64), axis=1, kind="stable")
+    assert np.mean(np.all(order == exact, axis=1)) >= 0.95

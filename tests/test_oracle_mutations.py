@@ -94,3 +94,45 @@ def test_sampler_mutants_are_caught():
     _fails(pins.check_temperature_matters, _mutant_sampler("no_temperature"))
     _fails(pins.check_lowest_index_tie, _mutant_sampler("last_tie"))
     pins.check_gumbel_law(osm.sample)
+
+
+def _mutant_philox(kind):
+    """Philox4x32 block functions with one plausible slip each."""
+    M0, M1 = osm.PHILOX_M
+    W0, W1 = osm.PHILOX_W
+    if kind == "swapped_multipliers":
+        M0, M1 = M1, M0
+    if kind == "swapped_weyl":
+        W0, W1 = W1, W0
+    rounds = 7 if kind == "seven_rounds" else 10
+
+    def block(counters, key):
+        out = []
+        for c0, c1, c2, c3 in np.asarray(counters, dtype=np.uint64).tolist():
+            k0, k1 = int(key[0]), int(key[1])
+            for r in range(rounds):
+                if r > 0 or kind == "bump_before_first":
+                    k0, k1 = (k0 + W0) & osm.MASK32, (k1 + W1) & osm.MASK32
+                p0, p1 = M0 * c0, M1 * c2
+                hi0, lo0 = p0 >> 32, p0 & osm.MASK32
+                hi1, lo1 = p1 >> 32, p1 & osm.MASK32
+                if kind == "hi_lo_swapped":
+                    hi0, lo0, hi1, lo1 = lo0, hi0, lo1, hi1
+                if kind == "key_words_swapped":
+                    c0, c1, c2, c3 = hi1 ^ c1 ^ k1, lo1, hi0 ^ c3 ^ k0, lo0
+                else:
+                    c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
+            out.append([c0, c1, c2, c3])
+        return np.array(out, dtype=np.uint64)
+    return block
+
+
+@pytest.mark.parametrize("kind", ["swapped_multipliers", "swapped_weyl", "seven_rounds",
+                                  "bump_before_first", "hi_lo_swapped", "key_words_swapped"])
+def test_philox_mutants_are_caught(kind):
+    _fails(pins.check_philox_kat, _mutant_philox(kind))
+
+
+def test_philox_mutant_harness_is_faithful():
+    # the mutant factory with no slip is the generator itself
+    pins.check_philox_kat(_mutant_philox("none"))

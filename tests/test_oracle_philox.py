@@ -1,6 +1,7 @@
-"""The oracle's counter-based noise.  Philox4x32-10 itself is parity unpinned
-(no known-answer vector); these checks constrain it by the algebra of its
-round, by output statistics, and by the Gumbel-max law of the draws."""
+"""The oracle's counter-based noise.  Philox4x32-10 is pinned to the published
+known-answer vectors (tests/golden/philox4x32_10_kat.json); the other checks
+constrain the stream built on it by the algebra of its round, by output
+statistics, and by the Gumbel-max law of the draws."""
 import numpy as np
 
 import pins
@@ -20,6 +21,10 @@ def _inverse_round(o, k0, k1):
         hi1 = (osm.PHILOX_M[1] * c2) >> 32
         out.append([c0, o0 ^ hi1 ^ k0, c2, o2 ^ hi0 ^ k1])
     return np.array(out, dtype=np.uint64)
+
+
+def test_known_answer_vectors():
+    pins.check_philox_kat(osm.philox4x32_10)
 
 
 def test_round_is_invertible():

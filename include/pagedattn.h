@@ -92,6 +92,19 @@ PKV_API const char* pkv_error_string(int code);
 PKV_API const char* pkv_status_string(uint32_t bits);
 
 /*
+ * Diagnostics (no counterpart on the pages).  Every in-kernel wait on a
+ * shared-memory barrier polls at most `polls` times, then gives up: the kernel
+ * sets PKV_STATUS_WAIT_TIMEOUT, lets the copies and tensor-core operations it
+ * already issued finish, frees what it holds and returns (its outputs are then
+ * unspecified).  The setting is process-wide and applies to calls enqueued
+ * after it.  The default, PKV_DEFAULT_WAIT_POLLS, is far beyond any wait of a
+ * healthy kernel; 0 makes every such wait give up at once, which is how the
+ * tests exercise the unwinding path.  Returns PKV_OK.
+ */
+#define PKV_DEFAULT_WAIT_POLLS (1u << 20)
+PKV_API int pkv_set_wait_poll_limit(uint32_t polls);
+
+/*
  * kv_store -- the per-layer KV cache write ("store_kvcache").
  * [UML] §2.4 (KV written into the cache before attention), §1 Step2 (slot =
  * blockID*blockSize + loc); [LIFE] §3.3.2 / §4 (slot_mapping holds one

@@ -17,7 +17,8 @@ from ._binding import (STATUS, cache_desc, kv_store, kv_store_paged_attention_va
                        paged_attention_varlen_workspace_bytes, layer_cache, library_path, load,
                        new_status, paged_decode, paged_decode_plan, paged_decode_run,
                        paged_decode_workspace_bytes, paged_prefill_varlen,
-                       paged_prefill_workspace_bytes, sample, sample_philox, status_names)
+                       paged_prefill_workspace_bytes, sample, sample_philox,
+                       set_wait_poll_limit, status_names)
 from ._build import build  # noqa: F401
 
 __all__ = ["kv_store", "paged_decode", "paged_prefill_varlen", "sample", "build", "load",
@@ -25,4 +26,4 @@ __all__ = ["kv_store", "paged_decode", "paged_prefill_varlen", "sample", "build"
            "kv_store_paged_attention_varlen", "paged_attention_varlen_workspace_bytes",
            "paged_decode_plan", "paged_decode_run", "sample_philox",
            "paged_decode_workspace_bytes", "paged_prefill_workspace_bytes", "new_status",
-           "status_names", "STATUS", "cache_desc", "library_path"]
+           "status_names", "STATUS", "cache_desc", "library_path", "set_wait_poll_limit"]

@@ -36,7 +36,7 @@ C_FUNCTIONS = ["pkv_version", "pkv_error_string", "pkv_status_string", "pkv_kv_s
                "pkv_kv_store_paged_prefill_varlen", "pkv_paged_decode_plan",
                "pkv_paged_decode_run", "pkv_paged_attention_varlen_workspace_bytes",
                "pkv_kv_store_paged_attention_varlen",
-               "pkv_layer_cache", "pkv_sample_philox"]
+               "pkv_layer_cache", "pkv_sample_philox", "pkv_set_wait_poll_limit"]
 
 # Size of the scratch array compiled into the library for
 # pkv_paged_decode_static_workspace (PKV_STATIC_DECODE_WORKSPACE_BYTES).
@@ -107,6 +107,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pkv_layer_cache.restype = ctypes.c_int
     lib.pkv_layer_cache.argtypes = [P, I32, I32, CacheDesc, ctypes.POINTER(ctypes.c_void_p),
                                     ctypes.POINTER(ctypes.c_void_p)]
+    lib.pkv_set_wait_poll_limit.restype = ctypes.c_int
+    lib.pkv_set_wait_poll_limit.argtypes = [ctypes.c_uint32]
     _LIB = lib
     return lib
 
@@ -490,3 +492,13 @@ def sample_philox(logits, temperatures, seed: int, offset: int, out=None, status
                                _stream(dev, stream))
     _check(rc, "pkv_sample_philox")
     return out
+
+
+DEFAULT_WAIT_POLLS = 1 << 20            # PKV_DEFAULT_WAIT_POLLS
+
+
+def set_wait_poll_limit(polls: int = DEFAULT_WAIT_POLLS) -> None:
+    """Polls a bounded in-kernel wait makes before it gives up, for calls
+    enqueued afterwards (default DEFAULT_WAIT_POLLS).  A diagnostic: 0 makes
+    every such wait give up at once, which exercises the kernels' unwinding."""
+    _check(load().pkv_set_wait_poll_limit(int(polls) & 0xFFFFFFFF), "pkv_set_wait_poll_limit")

@@ -15,6 +15,17 @@ int pkv_num_sms() {
     return cached[dev];
 }
 
+namespace {
+std::atomic<uint32_t> g_wait_polls{PKV_DEFAULT_WAIT_POLLS};
+}  // namespace
+
+uint32_t pkv_wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
+
+extern "C" int pkv_set_wait_poll_limit(uint32_t polls) {
+    g_wait_polls.store(polls, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
 extern "C" int pkv_version(void) { return 100; }
 
 extern "C" const char* pkv_error_string(int code) {

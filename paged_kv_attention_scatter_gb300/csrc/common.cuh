@@ -77,3 +77,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Host side: per-device SM count (cached).
 int pkv_num_sms();
+
+// Polls a bounded in-kernel mbarrier wait makes before it gives up (the
+// unwinding drains use their own, fixed limit).  pkv_set_wait_poll_limit
+// changes it for calls enqueued afterwards.
+uint32_t pkv_wait_polls();

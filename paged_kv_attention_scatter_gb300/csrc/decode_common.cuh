@@ -32,6 +32,7 @@ struct DecodeArgs {
     const int32_t* cu_k;
     int32_t total_q;                 // rows of q / out (varlen batch only)
     int32_t b0;                      // first sequence of a combine launch
+    uint32_t wait_polls;             // polls of a bounded mbarrier wait
 };
 
 // q / out row of sequence b

@@ -473,13 +473,16 @@ DecodeLayout decode_layout(int32_t batch, int32_t num_q_heads, int32_t max_ctx,
     return L;
 }
 
+// Resident CTAs per SM of the register-load split kernel, cached per device
+// (occupancy depends on the device's limits, so a process driving GPUs of
+// different kinds sizes each one's grid from its own answer).
 template <int D>
 int max_resident(const void* fn) {
-    static int cached[2] = {-1, -1};
+    static int cached[64][2] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    int& slot = cached[D == 128 ? 1 : 0];
-    if (slot < 0) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int& slot = cached[dev][D == 128 ? 1 : 0];
+    if (slot <= 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess ||
             n < 1)
@@ -578,6 +581,7 @@ int make_plan_args(const int32_t* context_lens, int32_t batch, int32_t num_q_hea
     a.cu_k = nullptr;
     a.total_q = 0;
     a.b0 = 0;
+    a.wait_polls = pkv_wait_polls();
     return PKV_OK;
 }
 

@@ -26,7 +26,11 @@
 //    or NaN cache contents never reach the output.  A block id outside the
 //    pool masks its stage and sets PKV_STATUS_BAD_BLOCK_ID.
 //  * Every wait on a barrier is bounded; on expiry the kernel sets
-//    PKV_STATUS_WAIT_TIMEOUT, lets the copies already issued land, and returns.
+//    PKV_STATUS_WAIT_TIMEOUT and returns.  The producer leaves last: it waits
+//    at a named barrier for the consumers to finish (normally or by giving
+//    up), and when any role gave up it lets every copy it issued land before
+//    the CTA can exit, since a consumer may give up after the producer has
+//    issued its last stage.
 #include <cudaTypedefs.h>
 
 #include "decode_common.cuh"
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t nh = min(kMaxGroup, a.G - hg * kMaxGroup);
             const int64_t qrow = qrow_of<kVarlen>(a, b);
             for (int32_t k = key0; k < key_end; k += kStageKeys) {
-                if (!tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag)) {
+                if (!tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag, a.wait_polls)) {
                     ok = false;
                     break;
                 }
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             u = un;
         }
-        if (ok && tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag)) {
+        if (ok && tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag, a.wait_polls)) {
             if (lane == 0) {
                 sm.meta[slot].flags = kEnd;
                 tc::mbar_arrive(&sm.full[slot]);
@@ -228,7 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm.abort_flag = 1;
                 pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
             }
-            // let every copy still in flight land before the CTA can exit
+        }
+        // wait until the consumers are done (they arrive at barrier 1 on every
+        // way out); if any role gave up, let every copy still in flight land
+        // before the CTA can exit
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+        if (sm.abort_flag) {
             for (int i = 1; i <= min(issued, S); ++i) {
                 int s = slot - i;
                 uint32_t ph = phase;
@@ -269,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t merged = 0;                         // units merged so far
     while (true) {
-        if (!tc::mbar_wait(&sm.full[slot], phase, &sm.abort_flag)) {
+        if (!tc::mbar_wait(&sm.full[slot], phase, &sm.abort_flag, a.wait_polls)) {
             if (lane == 0) {
                 sm.abort_flag = 1;
                 pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
@@ -371,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- end of a unit: merge the four warps (bounded mbarrier waits, so a
         // warp that gave up can never leave the others blocked) ----
-        if (merged > 0 && !tc::mbar_wait(&sm.merge_free, (merged - 1) & 1, &sm.abort_flag)) {
+        if (merged > 0 &&
+            !tc::mbar_wait(&sm.merge_free, (merged - 1) & 1, &sm.abort_flag, a.wait_polls)) {
             sm.abort_flag = 1;
             pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
             break;
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.o[warp][2 * t + 1][d_hi] = o[mt][3];
         }
         tc::mbar_arrive(&sm.merge_full);
-        if (!tc::mbar_wait(&sm.merge_full, merged & 1, &sm.abort_flag)) {
+        if (!tc::mbar_wait(&sm.merge_full, merged & 1, &sm.abort_flag, a.wait_polls)) {
             sm.abort_flag = 1;
             pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
             break;
@@ -426,6 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&sm.merge_free);
         ++merged;
     }
+    // the consumers are done: let the producer check for copies in flight
+    asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
 }
 
 template <int D>

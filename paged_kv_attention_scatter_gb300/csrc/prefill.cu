@@ -510,6 +510,7 @@ int pkv_prefill_make_args(const void* q, const void* k, const void* v, const voi
     a.scale_log2 = scale * pkv::kLog2e;
     a.status = status;
     a.skip_single = 0;
+    a.wait_polls = pkv_wait_polls();
     return PKV_OK;
 }
 

@@ -22,6 +22,7 @@ struct PrefillArgs {
     float scale_log2;
     uint32_t* status;
     int32_t skip_single;             // sequences of one query are left to the decode kernels
+    uint32_t wait_polls;             // polls of a bounded mbarrier wait
 };
 
 // Lengths of sequence b; returns false (and reports) when they are inconsistent.

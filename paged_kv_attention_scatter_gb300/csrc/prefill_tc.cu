@@ -54,9 +54,11 @@
 // Keeping P in TMEM means shared memory only carries Q, K and V: an SS MMA of
 // 128x128x16 already reads 128 bytes per clock from it.
 // TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512); stage,
-// S buffer and the barriers of tile t all use index t % 3.  Every mbarrier wait is bounded; a wait that gives up sets
-// PKV_STATUS_WAIT_TIMEOUT and the CTA unwinds, waits for its own copies and
-// MMAs, and frees TMEM.
+// S buffer and the barriers of tile t all use index t % 3.  Every mbarrier wait
+// is bounded; a wait that gives up sets PKV_STATUS_WAIT_TIMEOUT and the CTA
+// unwinds: the issuers wait for their MMAs, and after the CTA's last barrier
+// both producers (which may have finished normally) wait for every copy they
+// issued -- Q, K and V -- to land before TMEM is freed and the CTA exits.
 #include <cudaTypedefs.h>
 
 #include "prefill_common.cuh"
@@ -170,8 +172,9 @@ __device__ __forceinline__ void st_global_32b(void* p, const uint32_t (&w)[8]) {
 
 // All 32 lanes wait on the same barrier; the result is made warp-uniform so
 // the warp-wide TMEM instructions that follow never see a diverged warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const int* abort_flag) {
-    const bool r = mbar_wait(bar, parity, abort_flag);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const int* abort_flag,
+                                          uint32_t polls) {
+    const bool r = mbar_wait(bar, parity, abort_flag, polls);
     return __all_sync(0xffffffffu, r);
 }
 
@@ -179,12 +182,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // calls it when `warp_wide`, else one thread; the slot is released after the
 // read.
 template <class Smem>
-__device__ __forceinline__ bool next_item(Smem& s, uint32_t I, int32_t& it,
+__device__ __forceinline__ bool next_item(Smem& s, uint32_t I, int32_t& it, uint32_t polls,
                                           bool warp_wide = false) {
     const int qs = I % kItemRing;
     const uint32_t par = (I / kItemRing) & 1;
-    const bool got = warp_wide ? warp_wait(&s.item_full[qs], par, &s.abort_flag)
-                               : mbar_wait(&s.item_full[qs], par, &s.abort_flag);
+    const bool got = warp_wide ? warp_wait(&s.item_full[qs], par, &s.abort_flag, polls)
+                               : mbar_wait(&s.item_full[qs], par, &s.abort_flag, polls);
     if (!got) return false;
     it = s.item_ring[qs];
     if (warp_wide) {
@@ -301,6 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     const uint32_t tmem = s.tmem_base;
     asm volatile("griddepcontrol.wait;" ::: "memory");    // the plan's tile list
     const int64_t n_items = (int64_t)a.sched[0] * a.Hq;
+    // copies issued by this thread (a producer's lane 0), drained at the end
+    // if any role gave up: tiles into the ring, and Q tiles
+    uint32_t tiles_issued = 0, q_issued = 0;
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
@@ -312,14 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 tma_prefetch_desc(&maps.kc);
                 tma_prefetch_desc(&maps.vc);
             }
-            uint32_t T = 0, I = 0;
+            uint32_t& T = tiles_issued;
+            uint32_t I = 0;
             bool ok = true, bad_block = false;
             for (; ok; ++I) {
                 // the next item of the cost-sorted list, taken dynamically so
                 // the CTAs finish together; the other roles read it from the ring
                 const int qs = I % kItemRing;
                 if (I >= kItemRing &&
-                    !(ok = mbar_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1, &s.abort_flag)))
+                    !(ok = mbar_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1,
+                            &s.abort_flag, a.wait_polls)))
                     break;
                 const int32_t it = atomicAdd(&a.sched[1], 1);
                 s.item_ring[qs] = it < n_items ? it : -1;
@@ -327,15 +335,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 if (it >= n_items) break;
                 const Item x = item_at(a, it);
                 const int32_t kvh = x.h / a.G;
-                if (I > 0 && !(ok = mbar_wait(&s.q_free, (I - 1) & 1, &s.abort_flag))) break;
+                if (I > 0 && !(ok = mbar_wait(&s.q_free, (I - 1) & 1,
+                        &s.abort_flag, a.wait_polls))) break;
                 mbar_expect_tx(&s.q_full, kTile);
                 for (int hf = 0; hf < kBlocks; ++hf)
                     tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
                                 x.q0 + x.m * kBM);
+                ++q_issued;
                 for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
                     const int st = T % kStages;
                     const uint32_t use = T / kStages;
-                    if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_flag)))
+                    if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1,
+                            &s.abort_flag, a.wait_polls)))
                         break;
                     int32_t row, rows[kMaxBoxes];
                     const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
@@ -344,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                                          cached, row, rows, a.bs);
                     if constexpr (kBoxed) {
                         if (use > 0 &&
-                            !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag))) {
+                            !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
+                                    &s.abort_flag, a.wait_polls))) {
                             mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
                             break;
                         }
@@ -355,33 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 }
             }
             if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
-            if (!ok) {
-                give_up(s, a.status);
-                // let the copies already issued land before the CTA exits
-                for (int back = 1; back <= kStages && (int)T - back >= 0; ++back) {
-                    const uint32_t t = T - back;
-                    mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
-                    if (kBoxed) mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
-                }
-            }
+            if (!ok) give_up(s, a.status);
         }
     } else if (!kBoxed && warp == 7) {
         // ------------------------------------------------------------ V producer
         // V tiles on their own thread: a V stage waits for its P V, and in
         // the producer's loop that wait held back the next K tile
         if (lane == 0) {
-            uint32_t T = 0, I = 0;
+            uint32_t& T = tiles_issued;
+            uint32_t I = 0;
             bool ok = true, bad_block = false;
             for (; ok; ++I) {
                 int32_t it = -1;
-                if (!(ok = next_item(s, I, it))) break;
+                if (!(ok = next_item(s, I, it, a.wait_polls))) break;
                 if (it < 0) break;
                 const Item x = item_at(a, it);
                 const int32_t kvh = x.h / a.G;
                 for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
                     const int st = T % kStages;
                     const uint32_t use = T / kStages;
-                    if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag)))
+                    if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
+                            &s.abort_flag, a.wait_polls)))
                         break;
                     int32_t row, rows[kMaxBoxes];
                     const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
@@ -390,13 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                                          cached, row, rows, a.bs);
                 }
             }
-            if (!ok) {
-                give_up(s, a.status);
-                for (int back = 1; back <= kStages && (int)T - back >= 0; ++back) {
-                    const uint32_t t = T - back;
-                    mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
-                }
-            }
+            if (!ok) give_up(s, a.status);
         }
     } else if (warp == 5 || warp == 6) {
         // ------------------------------------------------------------ MMA issuers
@@ -412,18 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             bool ok = true;
             for (; ok; ++I) {
                 int32_t it = -1;
-                if (!(ok = next_item(s, I, it))) break;
+                if (!(ok = next_item(s, I, it, a.wait_polls))) break;
                 if (it < 0) break;
                 const Item x = item_at(a, it);
                 if (warp == 5) {
-                    if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag))) break;
+                    if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag, a.wait_polls))) break;
                     for (int32_t j = 0; j < x.n_tiles; ++j) {
                         const uint32_t t = T + j;
                         const int st = t % kStages;
-                        if (!(ok = mbar_wait(&s.k_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                        if (!(ok = mbar_wait(&s.k_full[st], (t / kStages) & 1,
+                                &s.abort_flag, a.wait_polls))) break;
                         // the S buffer still holds P of tile t-3 until its P V is done
                         if (t >= kStages &&
-                            !(ok = mbar_wait(&s.pv_done[st], (t / kStages - 1) & 1, &s.abort_flag)))
+                            !(ok = mbar_wait(&s.pv_done[st], (t / kStages - 1) & 1,
+                                    &s.abort_flag, a.wait_polls)))
                             break;
                         tc_fence_after();
                         const uint64_t kd = kd0 + (uint64_t)(st * (kTile >> 4));
@@ -442,10 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     for (int32_t j = 0; j < x.n_tiles; ++j) {
                         const uint32_t t = T + j;
                         const int st = t % kStages;
-                        if (!(ok = mbar_wait(&s.p_full[st], (t / kStages) & 1, &s.abort_flag))) break;
-                        if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1, &s.abort_flag)))
+                        if (!(ok = mbar_wait(&s.p_full[st], (t / kStages) & 1,
+                                &s.abort_flag, a.wait_polls))) break;
+                        if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1,
+                                &s.abort_flag, a.wait_polls)))
                             break;
-                        if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                        if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1,
+                                &s.abort_flag, a.wait_polls))) break;
                         tc_fence_after();
                         const uint64_t vd = vd0 + (uint64_t)(st * (kTile >> 4));
                         const uint32_t a_p = tmem + kColS0 + st * kBN;
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         bool ok = true;
         for (; ok; ++I) {
             int32_t it = -1;
-            if (!(ok = next_item(s, I, it, true))) break;
+            if (!(ok = next_item(s, I, it, a.wait_polls, true))) break;
             if (it < 0) break;
             const Item x = item_at(a, it);
             float m_run = -INFINITY, l_run = 0.f;
@@ -482,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 const uint32_t t = T + j;
                 const int st = t % kStages;
                 const uint32_t s_col = lane_base + kColS0 + st * kBN;
-                if (!(ok = warp_wait(&s.s_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                if (!(ok = warp_wait(&s.s_full[st], (t / kStages) & 1,
+                        &s.abort_flag, a.wait_polls))) break;
                 tc_fence_after();
                 float sv[kBN];
 #pragma unroll
@@ -566,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         // O may only be rescaled once the previous P V has finished
                         const uint32_t tp = t - 1;
                         if (!(ok = warp_wait(&s.pv_done[tp % kStages], (tp / kStages) & 1,
-                                             &s.abort_flag)))
+                                             &s.abort_flag, a.wait_polls)))
                             break;
                         tc_fence_after();
 #pragma unroll
@@ -585,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 tmem_wait_st();
                 if (partial_cached) {
                     // masked cached slots may hold NaN: zero their V rows
-                    if (!(ok = warp_wait(&s.v_full[st], (t / kStages) & 1, &s.abort_flag))) break;
+                    if (!(ok = warp_wait(&s.v_full[st], (t / kStages) & 1,
+                            &s.abort_flag, a.wait_polls))) break;
                     if (i >= lim) {
 #pragma unroll
                         for (int hf = 0; hf < kBlocks; ++hf)
@@ -603,7 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             if (!ok) break;
             // ---- epilogue: O / l to global ----
             const uint32_t tl = T + x.n_tiles - 1;
-            if (!(ok = warp_wait(&s.pv_done[tl % kStages], (tl / kStages) & 1, &s.abort_flag)))
+            if (!(ok = warp_wait(&s.pv_done[tl % kStages], (tl / kStages) & 1,
+                    &s.abort_flag, a.wait_polls)))
                 break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -652,6 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (s.abort_flag && lane == 0 && (warp == 4 || (!kBoxed && warp == 7))) {
+        // some role gave up: every copy this producer issued lands before the
+        // CTA exits (a consumer may have given up after the last one was issued)
+        const bool k_side = warp == 4;
+        for (uint32_t back = 1; back <= (uint32_t)kStages && back <= tiles_issued; ++back) {
+            const uint32_t t = tiles_issued - back;
+            if (k_side) mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
+            if (!k_side || kBoxed) mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
+        }
+        if (k_side && q_issued > 0) mbar_drain(&s.q_full, (q_issued - 1) & 1);
+    }
     if (warp == 5) tmem_dealloc(tmem, 512);
 }
 

@@ -42,8 +42,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `parity` to complete.  Gives up after `limit` polls
-// (each poll is itself a bounded hardware wait) and returns false; the caller
-// then records the failure and unwinds instead of spinning forever.
+// (each poll is itself a bounded hardware wait; 0 polls gives up at once) and
+// returns false; the caller then records the failure and unwinds instead of
+// spinning forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort_flag,
                                           uint32_t limit = (1u << 20)) {

@@ -37,8 +37,8 @@ L2_BYTES = 129e6
 LAYERS_0P6B = 28                   # decoder layers of a Qwen3-0.6B-shaped model
 
 # DRAM bytes (read + write) of one decode-0.6b paged_decode_run, summed over
-# its split and combine launches, from one ncu capture (profiles/
-# decode_tma_kernel_decode-0.6b.md).  Valid only for the decode sources it was
+# its split and combine launches, from one ncu capture of
+# `bench.py --profile decode-0.6b`.  Valid only for the decode sources it was
 # taken on: the digest below must match, otherwise the traffic is reported null.
 DECODE_0P6B_TRAFFIC = {"bytes": 582375168,
                        "sources_sha256": "4f3671be8474468ac0fcfe30a52d3b3b4518c9ca6ecf37f3d0b5debab6d14c9e"}
@@ -168,6 +168,31 @@ def time_graph(g, iters, torch):
     e.record()
     torch.cuda.synchronize()
     return s.elapsed_time(e) / iters * 1e-3          # seconds per replay
+
+
+def hbm_read_reference(torch, dev, nbytes=2 << 30, reps=10):
+    """A read-only stream for context beside the copy peak: the best of
+    `reps` torch reductions (sum and max) over a 2 GiB fp32 tensor, in GB/s
+    read.  The copy peak stays the roofline's denominator."""
+    x = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+    best = {}
+    for name, fn in (("sum", torch.sum), ("amax", torch.amax)):
+        fn(x)
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn(x)
+            e.record()
+            torch.cuda.synchronize()
+            t.append(s.elapsed_time(e) * 1e-3)
+        best[name] = nbytes / min(t) / 1e9
+    del x
+    torch.cuda.empty_cache()
+    name = max(best, key=best.get)
+    return {"gbs": round(best[name], 1), "how": f"torch.{name} over a 2 GiB fp32 tensor, best "
+            f"of {reps} (CUDA events; sum {best['sum']:.0f}, amax {best['amax']:.0f} GB/s)"}
 
 
 def flush_l2(buf):
@@ -346,6 +371,7 @@ def run_ours(args, rank, world, dist):
     del g, g1, q_h, out_h, layers, pool, kc0, vc0
     torch.cuda.empty_cache()
 
+    read_ref = hbm_read_reference(torch, dev)
     secondary = {"decode-0.6b-single-call": single}
     if not args.headline_only:
         secondary.update(run_secondary(args, pkv, W, torch, dev, pk))
@@ -373,7 +399,9 @@ def run_ours(args, rank, world, dist):
                      "traffic_unit": "bytes per paged_decode_run", "peak_source": pk["source"],
                      "kernel": "paged_decode_run (split-KV + combine launches), 28 per "
                                "step, plus one plan launch per step",
-                     "bytes_per_launch": nbytes / LAYERS_0P6B},
+                     "bytes_per_launch": nbytes / LAYERS_0P6B,
+                     "read_stream_reference": read_ref,
+                     "frac_of_read_stream": round(nbytes / step_s / 1e9 / read_ref["gbs"], 4)},
         "e2e": {"value": round(nbytes * world / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 5)},
@@ -646,50 +674,294 @@ def bench_step(pkv, W, torch, dev, pk):
 
 
 # ----------------------------------------------------------------------------
-# CPU oracle legs
+# CPU oracle legs: the oracle as it stands, timed on the host's cores
 # ----------------------------------------------------------------------------
-def oracle_worker(budget_s: float, steps: int, warmup: int, per_step: int):
-    """Times oracle.attention.paged_decode on whole sequences of decode-0.6b
-    (all q heads of `per_step` sequences per step), in a fresh interpreter with
-    single-threaded BLAS, stopping after `budget_s` seconds."""
+# The legs run in a fresh interpreter with CUDA hidden (started before any GPU
+# work of the benchmark).  Multi-core legs use one spawned worker process per
+# core of os.sched_getaffinity(0), each single-threaded (BLAS, OpenMP and torch
+# intra-op threads set to 1, so the cores are not oversubscribed), sharing the
+# inputs through shared memory; a unit of work (one sequence, one sampler row,
+# a set of prefill query rows) runs whole in one worker.  A leg dispatches
+# waves of units until its time budget is spent and reports the work done
+# over the wall time.
+_ORACLE_DATA: dict = {}
+
+
+def _oracle_pool_init(data):
+    import torch
+    torch.set_num_threads(1)
+    _ORACLE_DATA.update(data)
+
+
+def _oracle_unit(task):
+    """One unit of oracle work; returns its algorithmic amount (bytes or
+    FLOPs) so the caller can total what was done."""
     from oracle import attention as oatt
+    from oracle import sampler as osm
+    leg, i = task
+    d = _ORACLE_DATA[leg]
+    if leg == "prefill-8b":
+        s = d["units"][i]
+        oatt.paged_prefill_varlen(d["q"][s["b"]], d["k"][s["b"]], d["v"][s["b"]], d["k_cache"],
+                                  d["v_cache"], [0, s["lq"]], [0, s["lk"]], d["bt"][s["b"]],
+                                  d["scale"], rows={0: s["rows"]})
+        return s["flops"]
+    if leg == "step-8b sample":
+        osm.sample(d["logits"][i:i + 1], d["temps"][i:i + 1], d["noise"][i:i + 1])
+        return d["row_bytes"]
+    oatt.paged_decode(d["q"], d["k_cache"], d["v_cache"], d["bt"], d["ctx"], d["scale"],
+                      seqs=[i])
+    return d["unit_bytes"][i]
+
+
+def _decode_leg_data(spec, torch):
     from paged_kv_attention_scatter_gb300 import workloads as W
-
-    spec = W.DECODE_0P6B
     w = W.decode_workload(spec)
-    qf = w.q.double().numpy()
-    bt, ctx = w.block_tables.numpy(), w.context_lens.numpy()
-    B = spec.batch
+    ctx = w.context_lens.numpy()
+    return w, {"q": w.q.double().numpy(), "k_cache": w.k_cache.share_memory_(),
+               "v_cache": w.v_cache.share_memory_(), "bt": w.block_tables.numpy(), "ctx": ctx,
+               "scale": w.scale,
+               "unit_bytes": [decode_bytes([int(c)], spec.num_q_heads, spec.num_kv_heads,
+                                           spec.head_dim, spec.block_size) for c in ctx]}
 
-    def one_step(i):
-        nb = 0.0
-        for j in range(per_step):
-            b = (i * per_step + j) % B
-            oatt.paged_decode(qf, w.k_cache, w.v_cache, bt, ctx, w.scale, seqs=[b])
-            nb += decode_bytes([int(ctx[b])], spec.num_q_heads, spec.num_kv_heads,
-                               spec.head_dim, spec.block_size)
-        return nb
 
-    for i in range(warmup):
-        one_step(i)
-    t = time.perf_counter()
-    nbytes, done = 0.0, 0
-    for i in range(steps):
-        nbytes += one_step(warmup + i)
-        done += 1
-        if time.perf_counter() - t > budget_s:
+def _prefill_leg_data(spec, prompts: int, rows_per_unit: int):
+    """The first `prompts` prompts of prefill-8b (lengths and cached prefixes
+    drawn as the full workload draws them), computed in one chunk; a unit is
+    every n-th query row of one prompt."""
+    from dataclasses import replace
+
+    from paged_kv_attention_scatter_gb300 import workloads as W
+    g = W._gen(spec.seed)
+    lens = W.randint_incl(spec.len_lo, spec.len_hi, spec.num_prompts, g)
+    kbs = W.randint_incl(0, spec.max_cached_blocks, spec.num_prompts, g)
+    sub = replace(spec, num_prompts=prompts)
+    w = W.prefill_workload(sub, prompt_lens=lens[:prompts], cached_blocks=kbs[:prompts])
+    assert len(w.steps) == 1
+    st = w.steps[0]
+    cu_q, cu_k = st.cu_seqlens_q.tolist(), st.cu_seqlens_k.tolist()
+    q, k, v, bt, units = [], [], [], [], []
+    for b in range(prompts):
+        lq, lk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        q.append(st.q[cu_q[b]:cu_q[b + 1]].clone().share_memory_())
+        k.append(st.k[cu_q[b]:cu_q[b + 1]].clone().share_memory_())
+        v.append(st.v[cu_q[b]:cu_q[b + 1]].clone().share_memory_())
+        bt.append(st.block_tables[b:b + 1].numpy())
+        n_units = -(-lq // rows_per_unit)
+        for u in range(n_units):
+            rows = list(range(u, lq, n_units))
+            c = lk - lq
+            flops = 4.0 * spec.head_dim * spec.num_q_heads * sum(c + i + 1 for i in rows)
+            units.append({"b": b, "lq": lq, "lk": lk, "rows": rows, "flops": flops})
+    return {"q": q, "k": k, "v": v, "k_cache": w.k_cache0.share_memory_(),
+            "v_cache": w.v_cache0.share_memory_(), "bt": bt, "units": units,
+            "scale": w.scale, "tokens": cu_q[-1]}
+
+
+def _run_leg(pool, leg, n_units, cores, budget_s, warm_units=0):
+    """Waves of 2*cores units (cycling over the leg's units) until budget_s of
+    wall time; returns (amount done, units done, seconds, the unit indices
+    done)."""
+    nxt = 0
+    if warm_units:
+        pool.map(_oracle_unit, [(leg, (nxt + j) % n_units) for j in range(warm_units)],
+                 chunksize=1)
+        nxt += warm_units
+    amount, idx = 0.0, []
+    t0 = time.perf_counter()
+    while True:
+        wave = [(leg, (nxt + j) % n_units) for j in range(2 * cores)]
+        nxt += len(wave)
+        amount += sum(pool.map(_oracle_unit, wave, chunksize=1))
+        idx += [i for _, i in wave]
+        if time.perf_counter() - t0 > budget_s:
             break
-    el = time.perf_counter() - t
-    print(json.dumps({"value": nbytes / el / 1e9, "seconds": el, "steps": done,
-                      "seqs": done * per_step}))
+    return amount, len(idx), time.perf_counter() - t0, idx
 
 
-def cpu_oracle(steps, warmup, per_step, budget_s):
+def _one_core_tiny(budget_s: float):
+    """The whole tiny scenario (store + prefill with and without block tables,
+    three decode steps, the sampler) through the oracle on this one core."""
+    import torch
+
+    from oracle import attention as oatt
+    from oracle import kv_store as okv
+    from oracle import sampler as osm
+    from paged_kv_attention_scatter_gb300 import workloads as W
+    w = W.tiny_workload()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy()  # noqa: E731
+
+    def scenario():
+        p = w.prefill
+        kc, vc, _ = okv.kv_store(bits(p.k), bits(p.v), bits(w.k_cache0), bits(w.v_cache0),
+                                 p.slot_mapping.numpy())
+        kt, vt = torch.from_numpy(kc).view(torch.bfloat16), torch.from_numpy(vc).view(torch.bfloat16)
+        for bt in (p.block_tables.numpy(), None):
+            oatt.paged_prefill_varlen(p.q, p.k, p.v, kt, vt, p.cu_seqlens_q.numpy(),
+                                      p.cu_seqlens_k.numpy(), bt, w.scale)
+        for st in w.decode_steps:
+            kc, vc, _ = okv.kv_store(bits(st.k_new), bits(st.v_new), kc, vc,
+                                     st.slot_mapping.numpy())
+            kt = torch.from_numpy(kc).view(torch.bfloat16)
+            vt = torch.from_numpy(vc).view(torch.bfloat16)
+            oatt.paged_decode(st.q, kt, vt, st.block_tables.numpy(), st.context_lens.numpy(),
+                              w.scale)
+        osm.sample(w.logits.numpy(), w.temperatures.numpy(), w.exp_noise.numpy())
+
+    scenario()
+    n, t0 = 0, time.perf_counter()
+    while n < 3 or time.perf_counter() - t0 < budget_s:
+        scenario()
+        n += 1
+    return (time.perf_counter() - t0) / n, n
+
+
+def _one_core_decode(data, budget_s: float):
+    _oracle_pool_init({"decode-0.6b": data})
+    nb, n, t0 = 0.0, 0, time.perf_counter()
+    while n < 2 or time.perf_counter() - t0 < budget_s:
+        nb += _oracle_unit(("decode-0.6b", n % len(data["ctx"])))
+        n += 1
+    return nb, n, time.perf_counter() - t0
+
+
+def oracle_table(budget_s: float):
+    """Every leg of the CPU baseline; returns the JSON-ready table."""
+    import multiprocessing as mp
+
+    import torch
+    import torch.multiprocessing  # noqa: F401  (shared-memory tensor pickling)
+    from dataclasses import replace
+
+    from paged_kv_attention_scatter_gb300 import workloads as W
+    torch.set_num_threads(1)
+    cores = len(os.sched_getaffinity(0))
+    w06, d06 = _decode_leg_data(W.DECODE_0P6B, torch)
+    spec32 = replace(W.DECODE_32B, batch=16, num_blocks=None)
+    _, d32 = _decode_leg_data(spec32, torch)
+    spec_step = replace(W.STEP_8B, batch=32, vocab=None, store_new_token=False)
+    _, dstep = _decode_leg_data(spec_step, torch)
+    g = W._gen(W.STEP_8B.seed)
+    lg, tp, en = W.sampler_inputs(64, W.STEP_8B.vocab, W.STEP_8B.logit_sigma,
+                                  W.STEP_8B.logit_spikes, W.STEP_8B.t_lo, W.STEP_8B.t_hi, g)
+    dsamp = {"logits": lg.numpy(), "temps": tp.numpy(), "noise": en.numpy(),
+             "row_bytes": 8.0 * W.STEP_8B.vocab + 8}
+    dpre = _prefill_leg_data(W.PREFILL_8B, prompts=2, rows_per_unit=64)
+    data = {"decode-0.6b": d06, "decode-32b": d32, "step-8b decode": dstep,
+            "step-8b sample": dsamp, "prefill-8b": dpre}
+    one_dec = _one_core_decode(d06, budget_s * 0.5)
+    tiny_s, tiny_n = _one_core_tiny(budget_s * 0.25)
+    ctx = mp.get_context("spawn")
+    res = {}
+    with ctx.Pool(cores, initializer=_oracle_pool_init, initargs=(data,)) as pool:
+        for leg, n_units in (("decode-0.6b", len(d06["ctx"])), ("decode-32b", len(d32["ctx"])),
+                             ("step-8b decode", len(dstep["ctx"])),
+                             ("step-8b sample", dsamp["logits"].shape[0]),
+                             ("prefill-8b", len(dpre["units"]))):
+            res[leg] = _run_leg(pool, leg, n_units, cores, budget_s, warm_units=cores)
+    # the whole prefill-8b workload's FLOPs and new tokens, from its drawn
+    # prompt lengths and cached prefixes (chunking does not change the total)
+    sp = W.PREFILL_8B
+    g = W._gen(sp.seed)
+    lens = W.randint_incl(sp.len_lo, sp.len_hi, sp.num_prompts, g)
+    kbs = W.randint_incl(0, sp.max_cached_blocks, sp.num_prompts, g)
+    cached = [min(kb, (L - 1) // sp.block_size) * sp.block_size for L, kb in zip(lens, kbs)]
+    full_tokens = sum(L - c for L, c in zip(lens, cached))
+    full_flops = sum(prefill_flops([0, L - c], [0, L], sp.num_q_heads, sp.head_dim)
+                     for L, c in zip(lens, cached))
+    gbs = lambda r: round(r[0] / r[2] / 1e9, 4)  # noqa: E731
+    fl, n_pre, s_pre, idx_pre = res["prefill-8b"]
+    pre_rows = sum(len(dpre["units"][i]["rows"]) for i in idx_pre)
+    table = {
+        "cores": cores,
+        "decode-0.6b": {"value": gbs(res["decode-0.6b"]), "unit": "GB/s",
+                        "sample": f"{res['decode-0.6b'][1]} whole sequences (all 16 q heads) "
+                                  f"in {res['decode-0.6b'][2]:.1f} s"},
+        "decode-32b": {"value": gbs(res["decode-32b"]), "unit": "GB/s",
+                       "sample": f"{res['decode-32b'][1]} whole sequences of 16 drawn like "
+                                 f"decode-32b's (log-uniform contexts) in "
+                                 f"{res['decode-32b'][2]:.1f} s"},
+        "step-8b decode": {"value": gbs(res["step-8b decode"]), "unit": "GB/s",
+                           "sample": f"{res['step-8b decode'][1]} whole sequences of 32 drawn "
+                                     f"like step-8b's in {res['step-8b decode'][2]:.1f} s"},
+        "step-8b sample": {"value": gbs(res["step-8b sample"]), "unit": "GB/s",
+                           "rows_per_s": round(res["step-8b sample"][1] /
+                                               res["step-8b sample"][2], 2),
+                           "sample": f"{res['step-8b sample'][1]} rows of V=151936 in "
+                                     f"{res['step-8b sample'][2]:.1f} s"},
+        "prefill-8b": {"tflops": round(fl / s_pre / 1e12, 6),
+                       "tokens_per_s": round(pre_rows / s_pre, 2),
+                       "extrapolated_ms_for_workload": round(full_flops / (fl / s_pre) * 1e3, 1),
+                       "workload_tokens": full_tokens,
+                       "sample": f"{pre_rows} query rows (all 32 q heads; {n_pre} units of "
+                                 f"about 64 rows) of the first 2 prompts ({dpre['tokens']} new "
+                                 f"tokens) in "
+                                 f"{s_pre:.1f} s; the whole workload's time extrapolated by "
+                                 "FLOPs"},
+        "one_core": {
+            "decode-0.6b": {"value": round(one_dec[0] / one_dec[2] / 1e9, 4), "unit": "GB/s",
+                            "sample": f"{one_dec[1]} whole sequences in {one_dec[2]:.1f} s"},
+            "tiny": {"ms_per_scenario": round(tiny_s * 1e3, 2),
+                     "sample": f"{tiny_n} runs of the whole tiny scenario (store, prefill "
+                               "with and without tables, 3 decode steps, sampler)"}},
+    }
+    del w06
+    return table
+
+
+def oracle_worker(args):
+    """Entry of the fresh interpreter that runs the CPU legs; prints one JSON
+    line.  --budget is the seconds per multi-core leg."""
+    if args.reference_steps:
+        print(json.dumps(reference_waves(args.steps, args.warmup, args.budget)))
+    else:
+        print(json.dumps(oracle_table(args.budget)))
+
+
+def reference_waves(steps: int, warmup: int, budget_s: float):
+    """The reference arm: `steps` waves of decode-0.6b sequences, one per core
+    and wave, after `warmup` waves; stops early after budget_s seconds."""
+    import multiprocessing as mp
+
+    import torch
+    import torch.multiprocessing  # noqa: F401
+
+    from paged_kv_attention_scatter_gb300 import workloads as W
+    torch.set_num_threads(1)
+    cores = len(os.sched_getaffinity(0))
+    _, d06 = _decode_leg_data(W.DECODE_0P6B, torch)
+    n = len(d06["ctx"])
+    with mp.get_context("spawn").Pool(cores, initializer=_oracle_pool_init,
+                                      initargs=({"decode-0.6b": d06},)) as pool:
+        nxt = 0
+        for _ in range(warmup):
+            pool.map(_oracle_unit, [("decode-0.6b", (nxt + j) % n) for j in range(cores)],
+                     chunksize=1)
+            nxt += cores
+        amount, done = 0.0, 0
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            amount += sum(pool.map(_oracle_unit,
+                                   [("decode-0.6b", (nxt + j) % n) for j in range(cores)],
+                                   chunksize=1))
+            nxt += cores
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+    return {"value": amount / el / 1e9, "seconds": el, "steps": done, "seqs": done * cores,
+            "cores": cores}
+
+
+def cpu_oracle(budget_s: float, reference_steps: int = 0, warmup: int = 0):
+    """Runs the CPU legs in a fresh interpreter (no CUDA, one thread per
+    process) and returns its JSON."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker",
-           "--steps", str(steps), "--warmup", str(warmup), "--per-step", str(per_step),
            "--budget", str(budget_s)]
+    if reference_steps:
+        cmd += ["--reference-steps", "--steps", str(reference_steps), "--warmup", str(warmup)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
         raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
@@ -770,8 +1042,9 @@ def main():
                          "mixed, sample, kvstore")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-worker", action="store_true")
-    ap.add_argument("--per-step", type=int, default=1)
-    ap.add_argument("--budget", type=float, default=20.0)
+    ap.add_argument("--reference-steps", action="store_true")
+    ap.add_argument("--budget", type=float, default=6.0,
+                    help="seconds of wall time per multi-core CPU oracle leg")
     ap.add_argument("--profile", default=None,
                     help="run a small case for ncu instead of the benchmark: decode-0.6b, "
                          "prefill-8b, sample or mixed-8b (calls = --steps)")
@@ -783,7 +1056,7 @@ def main():
         return
 
     if args.oracle_worker:
-        oracle_worker(args.budget, args.steps, args.warmup, args.per_step)
+        oracle_worker(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -792,22 +1065,23 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        r = cpu_oracle(args.steps, min(args.warmup, 3), 1, budget_s=120.0)
+        warm = min(args.warmup, 3)
+        r = cpu_oracle(120.0, reference_steps=max(args.steps, 1), warmup=warm)
         from paged_kv_attention_scatter_gb300 import workloads as W
         spec = W.DECODE_0P6B
         ms = r["seconds"] / max(r["steps"], 1) * 1e3
+        sample = (f"{r['seqs']} whole sequences (all 16 q heads) of decode-0.6b, one per core "
+                  f"and step on {r['cores']} host cores (one spawned process each, float64 "
+                  "NumPy, single-threaded BLAS), at most 120 s")
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(r["value"], 4),
-            "unit": "GB/s", "n_gpus": 1, "steps": r["steps"], "warmup": min(args.warmup, 3),
+            "unit": "GB/s", "n_gpus": 1, "steps": r["steps"], "warmup": warm,
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": spec.name, "batch": spec.batch, "head_dim": spec.head_dim,
                        "block_size": spec.block_size},
-            "cpu_baseline": {"value": round(r["value"], 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle",
-                             "sample": f"{r['seqs']} whole sequences (all 16 q heads) of "
-                                       "decode-0.6b, one per step, float64 NumPy, "
-                                       "single-threaded BLAS, at most 120 s"},
+            "cpu_baseline": {"value": round(r["value"], 4), "unit": "GB/s",
+                             "cores": r["cores"], "kind": "oracle", "sample": sample},
             "e2e": {"value": round(r["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}))
         return
@@ -822,14 +1096,17 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # before any GPU work in this process: the oracle runs in a fresh interpreter
-        cpu = cpu_oracle(1000000, 2, 1, budget_s=15.0)
+        cpu = cpu_oracle(args.budget)
     res = run_ours(args, rank, world, dist)
     if cpu is not None:
-        res["cpu_baseline"] = {"value": round(cpu["value"], 4), "unit": "GB/s", "cores": 1,
-                               "kind": "oracle",
-                               "sample": f"{cpu['seqs']} whole sequences of decode-0.6b "
-                                         f"in {cpu['seconds']:.1f} s, float64 NumPy, "
-                                         "single-threaded BLAS"}
+        d06 = cpu.pop("decode-0.6b")
+        cores = cpu.pop("cores")
+        one = cpu.pop("one_core")
+        res["cpu_baseline"] = {
+            "value": d06["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": d06["sample"] + f" of decode-0.6b on {cores} host cores (one spawned "
+                      "process each, float64 NumPy, single-threaded BLAS)",
+            "one_core": one, "workloads": cpu}
     if rank == 0:
         print(json.dumps(res))
     if dist is not None:

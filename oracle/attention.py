@@ -90,11 +90,12 @@ def attend(q_rows: np.ndarray, keys: np.ndarray, values: np.ndarray,
 
 
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                 seqs=None) -> np.ndarray:
+                 seqs=None, heads=None) -> np.ndarray:
     """Decode attention ([UML] §2.4: the decode FA op reads K/V through
     block_tables with cache_seqlens; §3.2 formats): one query per sequence,
     attending all context_lens[b] cached keys.  Returns (B, Hq, D) float64;
-    rows of sequences not listed in `seqs` are NaN."""
+    rows of sequences not listed in `seqs` are NaN, and so are the q heads of
+    sequence b not listed in heads(b) when `heads` (a function of b) is given."""
     qf = _f64(q)
     B, Hq, D = qf.shape
     Hkv = k_cache.shape[2]
@@ -103,10 +104,11 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
     out = np.full((B, Hq, D), np.nan)
     for b in (range(B) if seqs is None else seqs):
         n = int(ctx[b])
+        hs = range(Hq) if heads is None else heads(b)
         if n == 0:
-            out[b] = 0.0
+            out[b, list(hs)] = 0.0
             continue
-        for h in range(Hq):
+        for h in hs:
             kvh = kv_head_of(h, Hq, Hkv)
             K = gather_keys(k_cache, bt[b], n, kvh)
             V = gather_keys(v_cache, bt[b], n, kvh)

@@ -13,7 +13,7 @@ from paged_kv_attention_scatter_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _decode(pkv, w, dev, seqs=None, status_expect=0, max_ctx=None):
+def _decode(pkv, w, dev, seqs=None, status_expect=0, max_ctx=None, heads=None):
     st = pkv.new_status(dev)
     out = pkv.paged_decode(w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev),
                            w.block_tables.to(dev), w.context_lens.to(dev), w.scale,
@@ -22,10 +22,21 @@ def _decode(pkv, w, dev, seqs=None, status_expect=0, max_ctx=None):
     kc = w.k_cache.cpu() if w.k_cache.is_cuda else w.k_cache
     vc = w.v_cache.cpu() if w.v_cache.is_cuda else w.v_cache
     ref = oatt.paged_decode(U.f64(w.q), kc, vc, w.block_tables.numpy(),
-                            w.context_lens.numpy(), w.scale, seqs=seqs)
+                            w.context_lens.numpy(), w.scale, seqs=seqs, heads=heads)
     got = U.f64(out)
     idx = list(range(w.q.shape[0])) if seqs is None else list(seqs)
-    return U.assert_close(got[idx], ref[idx], w.spec.name)
+    if heads is None:
+        return U.assert_close(got[idx], ref[idx], w.spec.name)
+    pairs = [(b, h) for b in idx for h in heads(b)]
+    bi, hi = np.array([p[0] for p in pairs]), np.array([p[1] for p in pairs])
+    return U.assert_close(got[bi, hi], ref[bi, hi], w.spec.name)
+
+
+def one_head_per_group(hq, hkv):
+    """q heads to check for sequence b: one per kv head, rotating through the
+    group with b, so that across sequences every q head is checked."""
+    g = hq // hkv
+    return lambda b: [kvh * g + (b + kvh) % g for kvh in range(hkv)]
 
 
 def test_tiny_decode_steps(cuda):
@@ -54,22 +65,31 @@ def test_decode_0p6b_full_batch(cuda):
     print(f"decode-0.6b: max abs {err:.3g}, rel L2 {rel:.3g}")
 
 
-def test_decode_32b_skewed_sampled(cuda):
+def test_decode_32b_every_sequence(cuda):
+    """All 256 sequences (contexts 128..32768, so every split/merge case of the
+    long rows), one q head per kv head each; the shortest and longest three
+    sequences with all 64 q heads."""
     pkv = U.lib()
     w = W.decode_workload(W.DECODE_32B, device=cuda)
-    ctx = w.context_lens.numpy()
-    order = np.argsort(ctx)
-    seqs = sorted(set(order[:3].tolist() + order[-3:].tolist() + [7, 100, 201]))
+    spec = W.DECODE_32B
+    err, rel = _decode(pkv, w, cuda, heads=one_head_per_group(spec.num_q_heads,
+                                                              spec.num_kv_heads))
+    print(f"decode-32b all sequences: max abs {err:.3g}, rel L2 {rel:.3g}")
+    order = np.argsort(w.context_lens.numpy())
+    seqs = sorted(set(order[:3].tolist() + order[-3:].tolist()))
     err, rel = _decode(pkv, w, cuda, seqs=seqs)
-    print(f"decode-32b sampled {seqs}: max abs {err:.3g}, rel L2 {rel:.3g}")
+    print(f"decode-32b all heads of {seqs}: max abs {err:.3g}, rel L2 {rel:.3g}")
 
 
-def test_step_8b_store_then_decode_sampled(cuda):
+def test_step_8b_store_then_decode_every_sequence(cuda):
+    """All 512 sequences of the step, one q head per kv head each (rotating),
+    after the step's kv_store wrote their newest token."""
     pkv = U.lib()
     w = W.decode_workload(W.STEP_8B, device=cuda)
     st = pkv.new_status(cuda)
     kc, vc = w.k_cache, w.v_cache
-    seqs = [0, 1, 77, 255, 300, 511]
+    seqs = list(range(W.STEP_8B.batch))
+    heads = one_head_per_group(W.STEP_8B.num_q_heads, W.STEP_8B.num_kv_heads)
     # oracle-side cache: the sequences' blocks before the step, then the store
     kc_cpu, vc_cpu = kc.cpu(), vc.cpu()
     pkv.kv_store(w.k_new, w.v_new, kc, vc, w.slot_mapping.to(cuda), status=st)
@@ -80,8 +100,11 @@ def test_step_8b_store_then_decode_sampled(cuda):
                              w.slot_mapping.numpy())
     ref = oatt.paged_decode(U.f64(w.q), torch.from_numpy(ok).view(torch.bfloat16),
                             torch.from_numpy(ov).view(torch.bfloat16), w.block_tables.numpy(),
-                            w.context_lens.numpy(), w.scale, seqs=seqs)
-    U.assert_close(U.f64(out)[seqs], ref[seqs], "step-8b decode")
+                            w.context_lens.numpy(), w.scale, seqs=seqs, heads=heads)
+    bi = np.repeat(np.array(seqs), W.STEP_8B.num_kv_heads)
+    hi = np.array([h for b in seqs for h in heads(b)])
+    err, rel = U.assert_close(U.f64(out)[bi, hi], ref[bi, hi], "step-8b decode")
+    print(f"step-8b all sequences: max abs {err:.3g}, rel L2 {rel:.3g}")
 
 
 # block sizes that are multiples of 64 run the TMA-fed split kernel, the others

@@ -158,11 +158,19 @@ def test_prefill_8b_steps_sampled_rows(cuda):
                                        step.max_seqlen_k, step.block_tables.to(cuda), w.scale,
                                        status=st)
         cu_q = step.cu_seqlens_q.numpy()
+        cu_k = step.cu_seqlens_k.numpy()
         rows = {}
         for b in range(len(cu_q) - 1):
             n = int(cu_q[b + 1] - cu_q[b])
+            c = int(cu_k[b + 1] - cu_k[b]) - n          # keys already cached
             pick = {0, n - 1, n // 2} | set(rng.integers(0, n, size=5).tolist())
-            rows[b] = sorted(pick)
+            # both sides of every 128-row query tile boundary (the kernel's
+            # work item), and the rows whose position ends a 128-key tile of
+            # the cached prefix or starts the next (the partial cached tile's
+            # mask and the first tile of the chunk's own keys)
+            pick |= {i for t in range(128, n, 128) for i in (t - 1, t)}
+            pick |= {i for i in range(n) if (c + i) % 128 in (0, 127)}
+            rows[b] = sorted(i for i in pick if 0 <= i < n)
         ref = oatt.paged_prefill_varlen(U.f64(step.q), U.f64(step.k), U.f64(step.v),
                                         torch.from_numpy(okc).view(torch.bfloat16),
                                         torch.from_numpy(ovc).view(torch.bfloat16),

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import gpu_util as U
+from oracle import attention as oatt
 from paged_kv_attention_scatter_gb300 import _binding
 from paged_kv_attention_scatter_gb300 import workloads as W
 
@@ -21,12 +22,19 @@ def _inputs(spec, dev):
 
 
 def _compare_with_workspace_entry_point(pkv, w, bt, ctx, dev):
+    """The static-workspace call against pkv_paged_decode (same kernels, so
+    bit for bit) and against the float64 oracle (within the attention
+    tolerance)."""
     ref = pkv.paged_decode(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale, w.max_context_len)
     st = pkv.new_status(dev)
     got = _binding.paged_decode_static_workspace(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale,
                                                  w.max_context_len, status=st)
     assert U.status_word(st) == 0
     U.assert_close(U.f64(got), U.f64(ref), "static-workspace decode vs workspace decode")
+    assert torch.equal(got, ref)
+    oracle = oatt.paged_decode(U.f64(w.q), w.k_cache.cpu(), w.v_cache.cpu(),
+                               w.block_tables.numpy(), w.context_lens.numpy(), w.scale)
+    U.assert_close(U.f64(got), oracle, "static-workspace decode vs the oracle")
 
 
 def test_two_calls_in_a_row_match_the_workspace_entry_point(cuda):

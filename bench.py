@@ -582,6 +582,30 @@ def bench_prefill(pkv, W, torch, dev, pk, flush):
             t_pre += e[1].elapsed_time(e[2]) * 1e-3
     t_store /= reps
     t_pre /= reps
+    # kv_store of the chunks on its own: (1) a CUDA graph of the five chunk
+    # stores back to back, replayed 20 times (each call's 128 MB of rows was last
+    # touched four calls, 512 MB of traffic, earlier: cold in L2), per-call mean;
+    # (2) the median of 20 single calls per chunk, each after an L2 flush, timed
+    # with CUDA events around the call (includes its launch latency)
+    gst = graph_of(lambda: [pkv.kv_store(t["k"], t["v"], kc, vc, t["slots"]) for t in steps],
+                   torch)
+    for _ in range(3):
+        gst.replay()
+    t_store_graph = time_graph(gst, 20, torch) / len(steps)
+    singles = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for t in steps:
+        per = []
+        for _ in range(20):
+            flush_l2(flush)
+            e0.record()
+            pkv.kv_store(t["k"], t["v"], kc, vc, t["slots"])
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e-3)
+        per.sort()
+        singles.append(per[len(per) // 2])
+    t_store_single = sum(singles) / len(singles)
     tokens = sum(t["q"].shape[0] for t in steps)
     flops = sum(t["flops"] for t in steps)
     store_bytes = sum(4 * t["k"].numel() * 2 for t in steps)
@@ -591,9 +615,18 @@ def bench_prefill(pkv, W, torch, dev, pk, flush):
         "tflops": round(flops / t_pre / 1e12, 2),
         "frac_tc_burst": round(flops / t_pre / 1e12 / pk["tc"], 4),
         "frac_tc_sustained": round(flops / t_pre / 1e12 / pk["tc_sustained"], 4),
-        "kv_store_gbs": round(store_bytes / t_store / 1e9, 1),
-        "kv_store_frac_hbm": round(store_bytes / t_store / 1e9 / pk["hbm"], 4),
-        "timing": "sum of per-call CUDA-event times over the chunk steps, L2 flushed "
+        "kv_store_gbs": round(store_bytes / len(steps) / t_store_graph / 1e9, 1),
+        "kv_store_frac_hbm": round(store_bytes / len(steps) / t_store_graph / 1e9 / pk["hbm"],
+                                   4),
+        "kv_store_us_per_chunk": round(t_store_graph * 1e6, 2),
+        "kv_store_single_call_median_us": round(t_store_single * 1e6, 2),
+        "kv_store_single_call_frac_hbm": round(store_bytes / len(steps) / t_store_single / 1e9
+                                               / pk["hbm"], 4),
+        "kv_store_timing": "kv_store_gbs: a CUDA graph of the 5 chunk stores back to back "
+                           "(640 MB of rows, each call's cold in L2), per-call mean of 20 "
+                           "replays; single_call: median of 20 calls per chunk, each after an "
+                           "L2 flush, CUDA events around the call (launch latency included)",
+        "timing": "prefill: sum of per-call CUDA-event times over the chunk steps, L2 flushed "
                   "before each step, mean of 3 passes"}
     del steps, kc, vc, w
     torch.cuda.empty_cache()
@@ -640,6 +673,7 @@ def bench_step(pkv, W, torch, dev, pk):
     gd = graph_of(lambda: pkv.paged_decode(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale,
                                            w.max_context_len, out=out, workspace=ws), torch)
     gm = graph_of(lambda: pkv.sample(logits, temps, noise, out=ids), torch)
+    gpx = graph_of(lambda: pkv.sample_philox(logits, temps, 1234, 0, out=ids), torch)
     gz = graph_of(lambda: pkv.kv_store_paged_decode(w.k_new, w.v_new, sl, w.q, w.k_cache,
                                                     w.v_cache, bt, ctx, w.scale,
                                                     w.max_context_len, out=out, workspace=ws),
@@ -651,12 +685,13 @@ def bench_step(pkv, W, torch, dev, pk):
                          out=out, workspace=ws)
         pkv.sample(logits, temps, noise, out=ids)
     gf = graph_of(full, torch)
-    for gg in (gs, gd, gm, gf, gz):
+    for gg in (gs, gd, gm, gf, gz, gpx):
         for _ in range(3):
             gg.replay()
     t_s, t_d, t_m, t_f = (time_graph(gs, 200, torch), time_graph(gd, 30, torch),
                           time_graph(gm, 50, torch), time_graph(gf, 30, torch))
     t_z = time_graph(gz, 30, torch)
+    t_px = time_graph(gpx, 50, torch)
     b_s = 4.0 * w.k_new.numel() * 2
     b_d = decode_bytes(w.context_lens.tolist(), spec.num_q_heads, spec.num_kv_heads,
                        spec.head_dim, spec.block_size)
@@ -669,6 +704,10 @@ def bench_step(pkv, W, torch, dev, pk):
         "fused_store_decode_us": round(t_z * 1e6, 2),
         "sample_us": round(t_m * 1e6, 2), "sample_gbs": round(b_m / t_m / 1e9, 1),
         "sample_frac_hbm": round(b_m / t_m / 1e9 / pk["hbm"], 4),
+        "sample_philox_us": round(t_px * 1e6, 2),
+        "sample_philox_gbs": round((b_m / 2) / t_px / 1e9, 1),
+        "sample_philox_note": "noise drawn in the kernel (Philox4x32-10): logits and "
+                              "temperatures only, 4 bytes per entry",
         "timing": "CUDA graph replays, CUDA events; kv_store re-writes the same slots"}
     return res
 

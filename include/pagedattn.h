@@ -228,9 +228,10 @@ PKV_API int pkv_paged_decode_static_workspace(
  * engine runs every decode step ([LIFE] §2.2.4: store_kvcache, then the
  * attention op; [UML] §2.4).  Arguments are those of pkv_kv_store (k, v,
  * slot_mapping, num_tokens) followed by those of pkv_paged_decode; k_cache
- * and v_cache are written by the store and read by the decode.  The decode's
- * set-up kernel is launched as a programmatic dependent of the store, so the
- * two overlap their launch latency; the attention still reads the stored rows.
+ * and v_cache are written by the store and read by the decode.  The store and
+ * the decode's set-up (its chunk schedule) run as one grid, so the pair costs
+ * one launch and the longer of the two; the attention kernels wait for that
+ * whole grid, so they read the stored rows whatever slots slot_mapping names.
  * Arguments are all checked before anything is enqueued.
  */
 PKV_API int pkv_kv_store_paged_decode(

@@ -48,6 +48,41 @@ __device__ __forceinline__ float4 ld_stream16f(const void* p) {
     return r;
 }
 
+// One kv_store call as a device-side row scatter: token i's K and V rows
+// (row_vecs 16-byte vectors each) go to pool row slots[i]; a negative slot is
+// a padding row, one past the pool is reported and skipped.
+struct StoreRows {
+    const uint4* k;
+    const uint4* v;
+    uint4* kc;
+    uint4* vc;
+    const int32_t* slots;
+    int32_t num_tokens, row_vecs;
+    int64_t num_slots;
+    uint32_t* status;
+};
+
+// The scatter over flat vector indices first, first + stride, ... (any split
+// of the grid; the index is divided by the row length).
+__device__ __forceinline__ void store_rows(const StoreRows& st, int64_t first, int64_t stride) {
+    const int64_t total = (int64_t)st.num_tokens * st.row_vecs;
+    for (int64_t idx = first; idx < total; idx += stride) {
+        const int32_t t = (int32_t)(idx / st.row_vecs);
+        const int32_t c = (int32_t)(idx - (int64_t)t * st.row_vecs);
+        const int32_t s = __ldg(st.slots + t);
+        if (s < 0) continue;
+        if ((int64_t)s >= st.num_slots) {
+            if (c == 0) report(st.status, PKV_STATUS_SLOT_OUT_OF_RANGE);
+            continue;
+        }
+        const uint4 kv = ld_stream16(st.k + idx);
+        const uint4 vv = ld_stream16(st.v + idx);
+        const int64_t dst = (int64_t)s * st.row_vecs + c;
+        st.kc[dst] = kv;
+        st.vc[dst] = vv;
+    }
+}
+
 // Two floats -> packed bf16x2 (round to nearest even), lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -77,6 +112,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Host side: per-device SM count (cached).
 int pkv_num_sms();
+
+// Checks pkv_kv_store's arguments and fills `st` (enqueues nothing); the
+// return code is the one pkv_kv_store gives for them.  num_tokens == 0 passes.
+int pkv_store_rows_args(const void* k, const void* v, void* k_cache, void* v_cache,
+                        const int32_t* slot_mapping, int32_t num_tokens,
+                        const pkv_cache_desc& cache, uint32_t* status, pkv::StoreRows& st);
 
 // Polls a bounded in-kernel mbarrier wait makes before it gives up (the
 // unwinding drains use their own, fixed limit).  pkv_set_wait_poll_limit

@@ -72,13 +72,15 @@ __global__ void __launch_bounds__(256) kv_store_kernel(
 
 }  // namespace
 
-extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
-                            const int32_t* slot_mapping, int32_t num_tokens,
-                            pkv_cache_desc cache, uint32_t* status, void* stream) {
+int pkv_store_rows_args(const void* k, const void* v, void* k_cache, void* v_cache,
+                        const int32_t* slot_mapping, int32_t num_tokens,
+                        const pkv_cache_desc& cache, uint32_t* status, pkv::StoreRows& st) {
     if (num_tokens < 0) return PKV_ERR_BAD_DIMENSION;
     if (cache.num_blocks <= 0 || cache.block_size <= 0 || cache.num_kv_heads <= 0 ||
         cache.head_dim <= 0)
         return PKV_ERR_BAD_DIMENSION;
+    st = pkv::StoreRows{};
+    st.num_tokens = num_tokens;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_NULL_POINTER;
     const int64_t row_bytes = (int64_t)cache.num_kv_heads * cache.head_dim * 2;
@@ -86,13 +88,31 @@ extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v
     if (((uintptr_t)k | (uintptr_t)v | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
         return PKV_ERR_MISALIGNED;
     if (((uintptr_t)slot_mapping) & 3) return PKV_ERR_MISALIGNED;
-    const int32_t row_vecs = (int32_t)(row_bytes / 16);
+    st.k = (const uint4*)k;
+    st.v = (const uint4*)v;
+    st.kc = (uint4*)k_cache;
+    st.vc = (uint4*)v_cache;
+    st.slots = slot_mapping;
+    st.row_vecs = (int32_t)(row_bytes / 16);
+    st.num_slots = (int64_t)cache.num_blocks * cache.block_size;
+    st.status = status;
+    return PKV_OK;
+}
+
+extern "C" int pkv_kv_store(const void* k, const void* v, void* k_cache, void* v_cache,
+                            const int32_t* slot_mapping, int32_t num_tokens,
+                            pkv_cache_desc cache, uint32_t* status, void* stream) {
+    pkv::StoreRows st;
+    const int rc = pkv_store_rows_args(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache,
+                                       status, st);
+    if (rc != PKV_OK || num_tokens == 0) return rc;
+    const int32_t row_vecs = st.row_vecs;
     const int64_t total = (int64_t)num_tokens * row_vecs;
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
     const int64_t cap = (int64_t)pkv_num_sms() * 16;
     if (blocks > cap) blocks = cap;
-    const int64_t num_slots = (int64_t)cache.num_blocks * cache.block_size;
+    const int64_t num_slots = st.num_slots;
     // the shift-and-mask form when a row is a power-of-two number of vectors
     // and every index fits in 32 bits (always, at these sizes)
     int shift = -1;

@@ -58,8 +58,10 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStep = 16;            // keys per warp step
 
-__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
-    allow_dependent_launch();
+// The chunk schedule of one decode batch, written by one CTA of up to 1024
+// threads: each sequence's chunk count as a prefix sum, and one record per
+// chunk (sequence, key range, chunk count).
+__device__ __forceinline__ void plan_body(const DecodeArgs& a) {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t carry;
     if (threadIdx.x == 0) carry = 0;
@@ -122,10 +124,27 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
         __syncthreads();
     }
     if (threadIdx.x == 0) a.chunk_prefix[0] = 0;
-    // When launched right after a kv_store (pkv_kv_store_paged_decode), finish
-    // only after the store has: the split kernel waits for this grid, so it
-    // then also sees the stored rows.  A no-op for an ordinary launch.
-    wait_for_predecessor();
+}
+
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a) {
+    allow_dependent_launch();
+    plan_body(a);
+}
+
+// kv_store and the decode plan as one grid (pkv_kv_store_paged_decode): block
+// 0 writes the chunk schedule while the other blocks store the step's K/V
+// rows, so the pair costs one launch and the longer of the two.  The split
+// kernel is this grid's programmatic dependent and waits for all of it, so it
+// reads the stored rows.
+__global__ void __launch_bounds__(1024) decode_store_plan_kernel(DecodeArgs a,
+                                                                 pkv::StoreRows st) {
+    allow_dependent_launch();
+    if (blockIdx.x == 0) {
+        plan_body(a);
+        return;
+    }
+    pkv::store_rows(st, (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x,
+                    (int64_t)(gridDim.x - 1) * blockDim.x);
 }
 
 template <int D>
@@ -492,16 +511,21 @@ int max_resident(const void* fn) {
     return slot;
 }
 
-// How a decode's plan kernel is launched: ordinarily, as a programmatic
-// dependent of a kv_store just enqueued, or not at all (a plan already in the
-// workspace).
-enum class PlanLaunch { kPlain, kAfterStore, kNone };
+// How a decode's plan kernel is launched: on its own, in one grid with the
+// step's kv_store (`store`), or not at all (a plan already in the workspace).
+enum class PlanLaunch { kPlain, kWithStore, kNone };
 
 template <int D>
-int launch_decode(DecodeArgs& a, cudaStream_t s, PlanLaunch plan = PlanLaunch::kPlain) {
-    if (plan == PlanLaunch::kAfterStore) {
-        if (launch_dependent(decode_plan_kernel, dim3(1), dim3(1024), s, a) != cudaSuccess)
-            return PKV_ERR_CUDA;
+int launch_decode(DecodeArgs& a, cudaStream_t s, PlanLaunch plan = PlanLaunch::kPlain,
+                  const pkv::StoreRows* store = nullptr) {
+    if (plan == PlanLaunch::kWithStore) {
+        // one vector per thread and tensor, blocks of 1024, at most 2 per SM
+        const int64_t vecs = (int64_t)store->num_tokens * store->row_vecs;
+        int64_t blocks = (vecs + 1023) / 1024;
+        const int64_t cap = 2LL * pkv_num_sms();
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        decode_store_plan_kernel<<<(unsigned)(1 + blocks), 1024, 0, s>>>(a, *store);
     } else if (plan == PlanLaunch::kPlain) {
         decode_plan_kernel<<<1, 1024, 0, s>>>(a);
     }
@@ -680,13 +704,15 @@ extern "C" int pkv_kv_store_paged_decode(
                               context_lens, batch, num_q_heads, max_context_len, scale, out,
                               workspace, workspace_bytes, cache, status, a);
     if (rc != PKV_OK) return rc;                 // nothing enqueued
-    rc = pkv_kv_store(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache, status, stream);
+    pkv::StoreRows st;
+    rc = pkv_store_rows_args(k, v, k_cache, v_cache, slot_mapping, num_tokens, cache, status,
+                             st);
     if (rc != PKV_OK) return rc;                 // nothing enqueued
     cudaStream_t s = (cudaStream_t)stream;
-    // an empty store launches nothing
-    const PlanLaunch plan = num_tokens > 0 ? PlanLaunch::kAfterStore : PlanLaunch::kPlain;
-    return cache.head_dim == 128 ? launch_decode<128>(a, s, plan)
-                                 : launch_decode<64>(a, s, plan);
+    // the store and the plan in one grid (an empty store: the plan alone)
+    const PlanLaunch plan = num_tokens > 0 ? PlanLaunch::kWithStore : PlanLaunch::kPlain;
+    return cache.head_dim == 128 ? launch_decode<128>(a, s, plan, &st)
+                                 : launch_decode<64>(a, s, plan, &st);
 }
 
 // ---------------------------------------------------------------------------

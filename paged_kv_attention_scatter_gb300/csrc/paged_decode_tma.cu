@@ -110,10 +110,14 @@ __device__ __forceinline__ int64_t qrow_of(const DecodeArgs& a, int32_t b) {
     return (int64_t)b;
 }
 
-template <int D, bool kVarlen>
+// kPolls: the waits take their poll limit from the arguments
+// (pkv_set_wait_poll_limit) rather than the compile-time default, in
+// instantiations of their own.
+template <int D, bool kVarlen, bool kPolls>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tma_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, DecodeArgs a) {
+    const uint32_t polls = kPolls ? a.wait_polls : (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t nh = min(kMaxGroup, a.G - hg * kMaxGroup);
             const int64_t qrow = qrow_of<kVarlen>(a, b);
             for (int32_t k = key0; k < key_end; k += kStageKeys) {
-                if (!tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag, a.wait_polls)) {
+                if (!tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag, polls)) {
                     ok = false;
                     break;
                 }
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             u = un;
         }
-        if (ok && tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag, a.wait_polls)) {
+        if (ok && tc::mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort_flag, polls)) {
             if (lane == 0) {
                 sm.meta[slot].flags = kEnd;
                 tc::mbar_arrive(&sm.full[slot]);
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t merged = 0;                         // units merged so far
     while (true) {
-        if (!tc::mbar_wait(&sm.full[slot], phase, &sm.abort_flag, a.wait_polls)) {
+        if (!tc::mbar_wait(&sm.full[slot], phase, &sm.abort_flag, polls)) {
             if (lane == 0) {
                 sm.abort_flag = 1;
                 pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- end of a unit: merge the four warps (bounded mbarrier waits, so a
         // warp that gave up can never leave the others blocked) ----
         if (merged > 0 &&
-            !tc::mbar_wait(&sm.merge_free, (merged - 1) & 1, &sm.abort_flag, a.wait_polls)) {
+            !tc::mbar_wait(&sm.merge_free, (merged - 1) & 1, &sm.abort_flag, polls)) {
             sm.abort_flag = 1;
             pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
             break;
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm.o[warp][2 * t + 1][d_hi] = o[mt][3];
         }
         tc::mbar_arrive(&sm.merge_full);
-        if (!tc::mbar_wait(&sm.merge_full, merged & 1, &sm.abort_flag, a.wait_polls)) {
+        if (!tc::mbar_wait(&sm.merge_full, merged & 1, &sm.abort_flag, polls)) {
             sm.abort_flag = 1;
             pkv::report(a.status, PKV_STATUS_WAIT_TIMEOUT);
             break;
@@ -448,11 +452,13 @@ int launch(DecodeArgs& a, cudaStream_t s) {
         !pkv::tma_encode_rows(&vmap, a.vc, rows, a.Hkv, D, kStageKeys))
         return PKV_ERR_CUDA;
     const int smem = (int)sizeof(DecodeSmem<D>) + 1024;
-    static std::atomic<uint64_t> configured[2] = {0, 0};
+    static std::atomic<uint64_t> configured[4] = {0, 0, 0, 0};
     const bool varlen = a.cu_q != nullptr;
+    const bool custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     void (*kernel)(const CUtensorMap, const CUtensorMap, DecodeArgs) =
-        varlen ? decode_tma_kernel<D, true> : decode_tma_kernel<D, false>;
-    if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[varlen ? 1 : 0]))
+        varlen ? (custom ? decode_tma_kernel<D, true, true> : decode_tma_kernel<D, true, false>)
+               : (custom ? decode_tma_kernel<D, false, true> : decode_tma_kernel<D, false, false>);
+    if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[(varlen ? 2 : 0) + custom]))
         return PKV_ERR_CUDA;
     int64_t grid = pkv_num_sms();
     const int64_t upper = (int64_t)a.cap * a.Hkv * a.n_hg;

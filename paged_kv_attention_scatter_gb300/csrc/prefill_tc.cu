@@ -265,10 +265,14 @@ __device__ __forceinline__ void load_tile(unsigned char* dst, const CUtensorMap*
 
 // kBoxed: the pool's blocks hold fewer than 128 keys, so a cached tile is
 // gathered from 128/bs boxes (a separate instantiation keeps the common
-// one-box producer loop free of that code).
-template <int D, bool kBoxed>
+// one-box producer loop free of that code).  kPolls: the waits take their
+// poll limit from the arguments (pkv_set_wait_poll_limit) instead of the
+// compile-time default, in instantiations of their own (a run-time limit in
+// the tight waits of the issuers cost the default kernel about 5%).
+template <int D, bool kBoxed, bool kPolls>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
+    const uint32_t polls = kPolls ? a.wait_polls : (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     constexpr int kTile = TcSmem<D>::kTile;
     constexpr int kBlocks = D / 64;               // 64-column blocks of a tile
     extern __shared__ unsigned char smem_raw[];
@@ -327,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 const int qs = I % kItemRing;
                 if (I >= kItemRing &&
                     !(ok = mbar_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1,
-                            &s.abort_flag, a.wait_polls)))
+                            &s.abort_flag, polls)))
                     break;
                 const int32_t it = atomicAdd(&a.sched[1], 1);
                 s.item_ring[qs] = it < n_items ? it : -1;
@@ -336,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 const Item x = item_at(a, it);
                 const int32_t kvh = x.h / a.G;
                 if (I > 0 && !(ok = mbar_wait(&s.q_free, (I - 1) & 1,
-                        &s.abort_flag, a.wait_polls))) break;
+                        &s.abort_flag, polls))) break;
                 mbar_expect_tx(&s.q_full, kTile);
                 for (int hf = 0; hf < kBlocks; ++hf)
                     tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     const int st = T % kStages;
                     const uint32_t use = T / kStages;
                     if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1,
-                            &s.abort_flag, a.wait_polls)))
+                            &s.abort_flag, polls)))
                         break;
                     int32_t row, rows[kMaxBoxes];
                     const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     if constexpr (kBoxed) {
                         if (use > 0 &&
                             !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
-                                    &s.abort_flag, a.wait_polls))) {
+                                    &s.abort_flag, polls))) {
                             mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
                             break;
                         }
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             bool ok = true, bad_block = false;
             for (; ok; ++I) {
                 int32_t it = -1;
-                if (!(ok = next_item(s, I, it, a.wait_polls))) break;
+                if (!(ok = next_item(s, I, it, polls))) break;
                 if (it < 0) break;
                 const Item x = item_at(a, it);
                 const int32_t kvh = x.h / a.G;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     const int st = T % kStages;
                     const uint32_t use = T / kStages;
                     if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
-                            &s.abort_flag, a.wait_polls)))
+                            &s.abort_flag, polls)))
                         break;
                     int32_t row, rows[kMaxBoxes];
                     const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
@@ -412,20 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             bool ok = true;
             for (; ok; ++I) {
                 int32_t it = -1;
-                if (!(ok = next_item(s, I, it, a.wait_polls))) break;
+                if (!(ok = next_item(s, I, it, polls))) break;
                 if (it < 0) break;
                 const Item x = item_at(a, it);
                 if (warp == 5) {
-                    if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag, a.wait_polls))) break;
+                    if (!(ok = mbar_wait(&s.q_full, I & 1, &s.abort_flag, polls))) break;
                     for (int32_t j = 0; j < x.n_tiles; ++j) {
                         const uint32_t t = T + j;
                         const int st = t % kStages;
                         if (!(ok = mbar_wait(&s.k_full[st], (t / kStages) & 1,
-                                &s.abort_flag, a.wait_polls))) break;
+                                &s.abort_flag, polls))) break;
                         // the S buffer still holds P of tile t-3 until its P V is done
                         if (t >= kStages &&
                             !(ok = mbar_wait(&s.pv_done[st], (t / kStages - 1) & 1,
-                                    &s.abort_flag, a.wait_polls)))
+                                    &s.abort_flag, polls)))
                             break;
                         tc_fence_after();
                         const uint64_t kd = kd0 + (uint64_t)(st * (kTile >> 4));
@@ -445,12 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         const uint32_t t = T + j;
                         const int st = t % kStages;
                         if (!(ok = mbar_wait(&s.p_full[st], (t / kStages) & 1,
-                                &s.abort_flag, a.wait_polls))) break;
+                                &s.abort_flag, polls))) break;
                         if (j == 0 && I > 0 && !(ok = mbar_wait(&s.o_free, (I - 1) & 1,
-                                &s.abort_flag, a.wait_polls)))
+                                &s.abort_flag, polls)))
                             break;
                         if (!(ok = mbar_wait(&s.v_full[st], (t / kStages) & 1,
-                                &s.abort_flag, a.wait_polls))) break;
+                                &s.abort_flag, polls))) break;
                         tc_fence_after();
                         const uint64_t vd = vd0 + (uint64_t)(st * (kTile >> 4));
                         const uint32_t a_p = tmem + kColS0 + st * kBN;
@@ -479,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         bool ok = true;
         for (; ok; ++I) {
             int32_t it = -1;
-            if (!(ok = next_item(s, I, it, a.wait_polls, true))) break;
+            if (!(ok = next_item(s, I, it, polls, true))) break;
             if (it < 0) break;
             const Item x = item_at(a, it);
             float m_run = -INFINITY, l_run = 0.f;
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 const int st = t % kStages;
                 const uint32_t s_col = lane_base + kColS0 + st * kBN;
                 if (!(ok = warp_wait(&s.s_full[st], (t / kStages) & 1,
-                        &s.abort_flag, a.wait_polls))) break;
+                        &s.abort_flag, polls))) break;
                 tc_fence_after();
                 float sv[kBN];
 #pragma unroll
@@ -572,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         // O may only be rescaled once the previous P V has finished
                         const uint32_t tp = t - 1;
                         if (!(ok = warp_wait(&s.pv_done[tp % kStages], (tp / kStages) & 1,
-                                             &s.abort_flag, a.wait_polls)))
+                                             &s.abort_flag, polls)))
                             break;
                         tc_fence_after();
 #pragma unroll
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 if (partial_cached) {
                     // masked cached slots may hold NaN: zero their V rows
                     if (!(ok = warp_wait(&s.v_full[st], (t / kStages) & 1,
-                            &s.abort_flag, a.wait_polls))) break;
+                            &s.abort_flag, polls))) break;
                     if (i >= lim) {
 #pragma unroll
                         for (int hf = 0; hf < kBlocks; ++hf)
@@ -611,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             // ---- epilogue: O / l to global ----
             const uint32_t tl = T + x.n_tiles - 1;
             if (!(ok = warp_wait(&s.pv_done[tl % kStages], (tl / kStages) & 1,
-                    &s.abort_flag, a.wait_polls)))
+                    &s.abort_flag, polls)))
                 break;
             tc_fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -685,10 +689,12 @@ template <int D>
 int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillPrologue* pre) {
     const int smem = (int)sizeof(TcSmem<D>) + 1024;
     const bool boxed = a.bt != nullptr && a.bs % kBN != 0;
-    static std::atomic<uint64_t> configured[2];
-    if (!pkv_dynamic_smem_once(boxed ? (const void*)prefill_tc_kernel<D, true>
-                                     : (const void*)prefill_tc_kernel<D, false>,
-                               smem, configured[boxed]))
+    const bool custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS;
+    void (*kernel)(const TcMaps, const PrefillArgs) =
+        boxed ? (custom ? prefill_tc_kernel<D, true, true> : prefill_tc_kernel<D, true, false>)
+              : (custom ? prefill_tc_kernel<D, false, true> : prefill_tc_kernel<D, false, false>);
+    static std::atomic<uint64_t> configured[4];
+    if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[(boxed ? 2 : 0) + custom]))
         return PKV_ERR_CUDA;
     a.tile_m = kBM;
     a.tile_n = kBN;
@@ -708,9 +714,7 @@ int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillP
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, boxed ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>,
-                           maps, a) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, maps, a) != cudaSuccess) return PKV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -24,6 +24,18 @@
 // (n / 4 as 64 bits, offset as 64 bits) for entry n = row * vocab + i, word
 // n % 4 of the four outputs; U = (word / 2^8 + 1) / 2^24 in (0, 1] and
 // E = -ln U.  The row then costs 4 bytes per entry instead of 8.
+//
+// There the two logarithms of the key, not the bytes, set the pace, so they
+// are computed only for entries that can still matter.  The key
+// x - ln(-ln U) grows with U, so an entry can reach a bound T0 only if
+// U >= exp(-exp(x - T0)).  Taking T0 a little below the best key the warp has
+// found so far, that threshold costs two fast exp2 evaluations; it is lowered
+// by margins larger than its own error (about 1e-5 relative), and the word is
+// compared with room for its float conversion, so the test never turns away
+// an entry whose exact key reaches the warp's best.  Entries that pass get the
+// exact key (the same float formula as with supplied noise), so the chosen
+// token is the one the unfiltered computation picks.  After a row's first
+// few entries almost none pass.
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
@@ -56,20 +68,6 @@ __device__ __forceinline__ float gumbel_key(float logit, float inv_t, float e) {
 constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r > 0) {
-            k0 += kPhiloxW0;
-            k1 += kPhiloxW1;
-        }
-        const uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
-        const uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    }
-    return c;
-}
-
 // Exp(1) noise from one Philox output word: U = (w / 2^8 + 1) / 2^24, E = -ln U.
 // logf (not the fast log): U close to 1 gives a tiny E that needs relative accuracy.
 __device__ __forceinline__ float exp_noise_of(uint32_t w) {
@@ -77,14 +75,78 @@ __device__ __forceinline__ float exp_noise_of(uint32_t w) {
     return -logf(u);
 }
 
-__device__ __forceinline__ uint4 philox_block(uint64_t n4, uint64_t seed, uint64_t offset) {
-    return philox4x32_10(make_uint4((uint32_t)n4, (uint32_t)(n4 >> 32), (uint32_t)offset,
-                                    (uint32_t)(offset >> 32)),
-                         (uint32_t)seed, (uint32_t)(seed >> 32));
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& w, int j) {
     return j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+}
+
+// The key schedule of one seed, computed once per thread: round r uses the
+// seed's two words plus r times the Weyl increments.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        k.k0[r] = a;
+        k.k1[r] = b;
+        a += kPhiloxW0;
+        b += kPhiloxW1;
+    }
+    return k;
+}
+
+// Philox4x32-10 of counter (n4 low, n4 high, offset low, offset high): each
+// round multiplies words 0 and 2 by the two constants and mixes the products'
+// high words with words 1 and 3 and the round key.
+__device__ __forceinline__ uint4 philox_block_keys(uint64_t n4, uint64_t offset,
+                                                   const PhiloxKeys& k) {
+    uint4 c = make_uint4((uint32_t)n4, (uint32_t)(n4 >> 32), (uint32_t)offset,
+                         (uint32_t)(offset >> 32));
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(kPhiloxM0, c.x), lo0 = kPhiloxM0 * c.x;
+        const uint32_t hi1 = __umulhi(kPhiloxM1, c.z), lo1 = kPhiloxM1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0);
+    }
+    return c;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Order-preserving map of floats (not NaN) to signed ints, and back.
+__device__ __forceinline__ int ordered(float f) {
+    const int i = __float_as_int(f);
+    return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ float unordered(int i) {
+    return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// The smallest Philox word with which an entry of scaled logit x (or any
+// smaller one) may still reach a key T0, given a = (x - T0) * log2(e).
+// Exactly: U >= thr = exp(-exp(x - T0)), and U = (w/2^8 + 1) / 2^24 makes that
+// w >= thr * 2^32 - 256.  thr comes from two fast exp2 (relative error below
+// 2e-5 wherever thr * 2^32 exceeds 512), is lowered by the factor 2^(-1/4096)
+// (1.7e-4) and truncated to an integer, and 512 more is taken off (0 if that
+// goes below 0), so the bound never exceeds the exact one.  An entry with a
+// smaller x needs a larger U, so the bound of a block's largest x serves the
+// whole block.  A NaN exponent gives 0 (every word passes: the exact key
+// decides); +inf gives 0 as well.
+__device__ __forceinline__ uint32_t reach_floor(float a) {
+    const float z = fast_exp2(a);                                      // exp(x - T0)
+    const float thr32 = fast_exp2(fmaf(z, -kLog2e, 32.0f - 1.0f / 4096.0f));
+    uint32_t t;
+    asm("cvt.rzi.sat.u32.f32 %0, %1;" : "=r"(t) : "f"(thr32));          // NaN -> 0
+    return t > 512u ? t - 512u : 0u;
 }
 
 template <bool kPhilox>
@@ -100,6 +162,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
     __shared__ int warp_idx[kThreads / 32];
     __shared__ Cand cta_best[2];          // by row parity: one cluster barrier per row
 
+    const PhiloxKeys keys = philox_keys(kPhilox ? seed : 0);
     // persistent: a cluster per resident slot walks rows blockIdx.y, +gridDim.y, ...
     int par = 0;
     for (int64_t row = blockIdx.y; row < num_rows; row += gridDim.y, par ^= 1) {
@@ -141,25 +204,66 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
                     }
                 }
             }
-            for (int v = v0; v < nvec; v += kThreads) {
-                const int i = lo + 4 * v;
-                const float4 l4 = pkv::ld_stream16f(lrow + i);
-                float4 e4;
-                if (kPhilox) {
-                    const uint4 w = philox_block((n_row + i) >> 2, seed, offset);
-                    e4 = make_float4(exp_noise_of(w.x), exp_noise_of(w.y), exp_noise_of(w.z),
-                                     exp_noise_of(w.w));
-                } else {
-                    e4 = pkv::ld_stream16f(nrow + i);
+            if constexpr (kPhilox) {
+                // warp-uniform trip count (the warp's best is a warp-wide
+                // reduction); lane l of warp w takes vectors 32w + l, + 256, ...
+                const int lane = threadIdx.x & 31;
+                const float c1 = inv_t * kLog2e;
+                float wbest = -CUDART_INF_F;               // best key of the warp so far
+                int vb = threadIdx.x & ~31;
+                float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (vb + lane < nvec) l4 = pkv::ld_stream16f(lrow + lo + 4 * (vb + lane));
+                for (; vb < nvec; vb += kThreads) {
+                    const int v = vb + lane;
+                    const bool in = v < nvec;
+                    const int i = lo + 4 * v;
+                    // the next vector's logits in flight while this one is done
+                    const int vn = v + kThreads;
+                    float4 l4n = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (vn < nvec) l4n = pkv::ld_stream16f(lrow + lo + 4 * vn);
+                    const uint4 w = philox_block_keys((n_row + (uint64_t)i) >> 2, offset, keys);
+                    // T0 a little below the warp's best: the formula's own
+                    // rounding (about 1e-6 of the key) stays inside it
+                    const float t0 = wbest - (1e-3f + 1e-4f * fabsf(wbest));
+                    const float c0 = -t0 * kLog2e;
+                    const float lj[4] = {l4.x, l4.y, l4.z, l4.w};
+                    // one bound for the block, from its largest logit (NaN
+                    // entries are ignored by the max; a block of NaN passes)
+                    const float lmax = fmaxf(fmaxf(l4.x, l4.y), fmaxf(l4.z, l4.w));
+                    // nothing taken yet: every entry gets the exact key
+                    const uint32_t floor_w =
+                        best.idx == INT_MAX ? 0u : reach_floor(fmaf(lmax, c1, c0));
+                    uint32_t cand = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cand |= (uint32_t)(word_of(w, j) >= floor_w) << j;
+                    if (!in) cand = 0;
+                    // the exact keys, one passing entry at a time (a loop
+                    // with a data-dependent count, so the two logarithms are
+                    // branched over rather than predicated in every lane)
+                    while (cand) {
+                        const int j = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        const float lv = j == 0 ? lj[0] : j == 1 ? lj[1] : j == 2 ? lj[2] : lj[3];
+                        take_if_better(best, gumbel_key(lv, inv_t, exp_noise_of(word_of(w, j))),
+                                       i + j);
+                    }
+                    wbest = unordered(__reduce_max_sync(0xffffffffu, ordered(best.key)));
+                    l4 = l4n;
                 }
-                take_if_better(best, gumbel_key(l4.x, inv_t, e4.x), i);
-                take_if_better(best, gumbel_key(l4.y, inv_t, e4.y), i + 1);
-                take_if_better(best, gumbel_key(l4.z, inv_t, e4.z), i + 2);
-                take_if_better(best, gumbel_key(l4.w, inv_t, e4.w), i + 3);
+            } else {
+                for (int v = v0; v < nvec; v += kThreads) {
+                    const int i = lo + 4 * v;
+                    const float4 l4 = pkv::ld_stream16f(lrow + i);
+                    const float4 e4 = pkv::ld_stream16f(nrow + i);
+                    take_if_better(best, gumbel_key(l4.x, inv_t, e4.x), i);
+                    take_if_better(best, gumbel_key(l4.y, inv_t, e4.y), i + 1);
+                    take_if_better(best, gumbel_key(l4.z, inv_t, e4.z), i + 2);
+                    take_if_better(best, gumbel_key(l4.w, inv_t, e4.w), i + 3);
+                }
             }
             for (int i = lo + 4 * nvec + threadIdx.x; i < hi; i += kThreads) {
                 const float e = kPhilox ? exp_noise_of(word_of(
-                                              philox_block((n_row + i) >> 2, seed, offset),
+                                              philox_block_keys((n_row + i) >> 2, offset, keys),
                                               (int)((n_row + i) & 3)))
                                         : nrow[i];
                 take_if_better(best, gumbel_key(lrow[i], inv_t, e), i);
@@ -167,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
         } else {
             for (int i = lo + threadIdx.x; i < hi; i += kThreads) {
                 const float e = kPhilox ? exp_noise_of(word_of(
-                                              philox_block((n_row + i) >> 2, seed, offset),
+                                              philox_block_keys((n_row + i) >> 2, offset, keys),
                                               (int)((n_row + i) & 3)))
                                         : nrow[i];
                 take_if_better(best, gumbel_key(lrow[i], inv_t, e), i);
@@ -215,36 +319,25 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
     cluster.sync();                       // keep shared memory alive for rank 0
 }
 
+// Clusters of `csize` CTAs of sample_kernel<kPhilox> that fit on the current
+// device at once, cached per device (65535 if the query fails).
 template <bool kPhilox>
-int launch_sample(const float* logits, const float* temperatures, const float* exp_noise,
-                  uint64_t seed, uint64_t offset, int32_t batch, int32_t vocab,
-                  int32_t* out_token_ids, uint32_t* status, void* stream) {
-    const bool vec_ok = (vocab % 4 == 0) &&
-                        ((((uintptr_t)logits) | ((uintptr_t)exp_noise)) & 15) == 0;
-    int csize = (vocab + 16383) / 16384;           // about 16K entries per CTA
-    // at most 8 CTAs per row reading the noise, 4 drawing it (the ALU-bound
-    // Philox kernel gains from twice as many resident clusters: B=512 x
-    // V=151936 160 -> 149 us; with supplied noise 4 measured 2% slower)
-    const int max_csize = kPhilox ? 4 : 8;
-    if (csize > max_csize) csize = max_csize;
-    if (csize < 1) csize = 1;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)csize, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = (cudaStream_t)stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // as many clusters as can be resident at once (no partial last wave),
-    // each walking rows; queried once per cluster size
-    static int resident[2][9] = {};
-    int& n_res = resident[kPhilox ? 1 : 0][csize];
+int resident_clusters(int csize) {
+    static int cache[64][9] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int& n_res = cache[dev][csize];
     if (n_res == 0) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)csize;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)csize, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, sample_kernel<kPhilox>, &cfg) != cudaSuccess ||
             n < 1) {
@@ -253,8 +346,58 @@ int launch_sample(const float* logits, const float* temperatures, const float* e
         }
         n_res = n;
     }
+    return n_res;
+}
+
+template <bool kPhilox>
+int launch_sample(const float* logits, const float* temperatures, const float* exp_noise,
+                  uint64_t seed, uint64_t offset, int32_t batch, int32_t vocab,
+                  int32_t* out_token_ids, uint32_t* status, void* stream) {
+    const bool vec_ok = (vocab % 4 == 0) &&
+                        ((((uintptr_t)logits) | ((uintptr_t)exp_noise)) & 15) == 0;
+    int csize;
+    if (!kPhilox) {
+        // reading the noise is bandwidth-bound: about 16K entries per CTA, at
+        // most 8 CTAs per row
+        csize = (vocab + 16383) / 16384;
+        if (csize > 8) csize = 8;
+        if (csize < 1) csize = 1;
+    } else {
+        // drawing it is arithmetic-bound, so a partial last wave of clusters
+        // costs time in proportion: take the cluster size c (at most 8, at
+        // least 4096 entries per CTA) with the fewest waves of row segments,
+        // ceil(batch / resident clusters(c)) / c; ties go to the larger c
+        // (B=512 x V=151936: 8 CTAs per SM give 1216 CTA slots, and c = 7 runs
+        // 3 waves of 1/7 rows where c = 4 runs 2 of 1/4)
+        int c_max = (vocab + 4095) / 4096;
+        if (c_max > 8) c_max = 8;
+        if (c_max < 1) c_max = 1;
+        csize = 1;
+        double best = 1e30;
+        for (int c = 1; c <= c_max; ++c) {
+            const int n = resident_clusters<true>(c);
+            const double waves = (double)((batch + n - 1) / n);
+            const double cost = waves / c;
+            if (cost <= best * (1.0 + 1e-9)) {
+                best = cost;
+                csize = c;
+            }
+        }
+    }
+    const int n_res = resident_clusters<kPhilox>(csize);
     const int32_t clusters = batch < n_res ? batch : n_res;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)csize, (unsigned)clusters, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = (cudaStream_t)stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel<kPhilox>, logits, temperatures,
                                        exp_noise, seed, offset, batch, vocab, vec_ok,
                                        out_token_ids, status);

@@ -25,18 +25,46 @@ def test_equal_logits_pick_the_largest_word_exactly(cuda, vocab, seed, offset):
     assert np.array_equal(ids, np.argmax(w, axis=1))
 
 
-def test_spiked_logits_full_vocab_rows(cuda):
+@pytest.mark.parametrize("t_lo,t_hi", [(0.2, 1.2), (0.02, 0.2), (1.2, 4.0)])
+def test_spiked_logits_full_vocab_rows(cuda, t_lo, t_hi):
+    """Full 151936-entry rows of the step-8b sampler inputs at low, step-8b and
+    high temperatures (the kernel computes the exact key only for entries that
+    can still reach its running best, a share that depends on the spread)."""
     pkv = U.lib()
+    B = 24
     g = torch.Generator().manual_seed(4)
-    logits, temps, _ = W.sampler_inputs(12, 151936, 3.0, 4, 0.2, 1.2, g)
+    logits, temps, _ = W.sampler_inputs(B, 151936, 3.0, 4, t_lo, t_hi, g)
     ids = pkv.sample_philox(logits.to(cuda), temps.to(cuda), 99, 5).cpu().numpy()
     ref, bad = osm.sample_philox(logits.numpy(), temps.numpy(), 99, 5)
-    E = osm.philox_exp_noise(12, 151936, 99, 5)
+    E = osm.philox_exp_noise(B, 151936, 99, 5)
     _, keys = osm.sample_key_form(logits.numpy(), temps.numpy(), E)
     near = osm.near_ties(keys)
     assert not bad
-    for r in range(12):
+    for r in range(B):
         assert ids[r] == ref[r] or (len(near[r]) > 1 and ids[r] in near[r])
+
+
+def test_degenerate_rows(cuda):
+    """Rows where only a few entries (or none) have a finite key: every key
+    -inf gives the lowest index; one finite logit, or one +inf logit, wins; a
+    row of NaN gives 0 and reports PKV_STATUS_NO_FINITE_KEY; a row of equal
+    logits with one raised entry far above the rest picks that entry."""
+    pkv = U.lib()
+    V = 5003
+    lg = torch.zeros(5, V)
+    lg[0] = float("-inf")
+    lg[1] = float("-inf")
+    lg[1, 4321] = 0.0
+    lg[2] = float("nan")
+    lg[3] = float("-inf")
+    lg[3, 17] = float("inf")
+    lg[4] = 0.0
+    lg[4, 2999] = 200.0
+    temps = torch.tensor([1.0, 0.5, 1.0, 1.0, 0.7])
+    st = pkv.new_status(cuda)
+    ids = pkv.sample_philox(lg.to(cuda), temps.to(cuda), 5, 6, status=st).cpu().tolist()
+    assert ids == [0, 4321, 0, 17, 2999]
+    assert U.status_word(st) == pkv.STATUS["NO_FINITE_KEY"]
 
 
 def test_draws_follow_the_gumbel_law(cuda):

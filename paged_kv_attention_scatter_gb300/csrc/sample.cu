@@ -90,8 +90,10 @@ __device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
     uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        k.k0[r] = a;
-        k.k1[r] = b;
+        // kept in registers (an opaque copy is not recomputed at each use,
+        // which would cost an add per round and key)
+        asm volatile("mov.b32 %0, %1;" : "=r"(k.k0[r]) : "r"(a));
+        asm volatile("mov.b32 %0, %1;" : "=r"(k.k1[r]) : "r"(b));
         a += kPhiloxW0;
         b += kPhiloxW1;
     }
@@ -130,6 +132,16 @@ __device__ __forceinline__ float unordered(int i) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+// The smallest noise term of any key: -ln E >= -ln(24 ln 2) = -2.8116 because
+// U >= 2^-24 gives E = -ln U <= 24 ln 2.  Rounded up.
+constexpr float kMinBonus = 2.8117f;
+
+__device__ __forceinline__ float max4(const float4& v) {
+    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+}
+__device__ __forceinline__ uint32_t max4u(const uint4& w) {
+    return max(max(w.x, w.y), max(w.z, w.w));
+}
 
 // The smallest Philox word with which an entry of scaled logit x (or any
 // smaller one) may still reach a key T0, given a = (x - T0) * log2(e).
@@ -149,8 +161,20 @@ __device__ __forceinline__ uint32_t reach_floor(float a) {
     return t > 512u ? t - 512u : 0u;
 }
 
+// The exact keys of the entries of one block whose word reaches `floor_w`
+// (called behind a test that some word does, which is rare once a row's best
+// has settled).
+__device__ __forceinline__ void exact_block(Cand& best, const float4& l, const uint4& w,
+                                            uint32_t floor_w, float inv_t, int i0) {
+    const float lj[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (word_of(w, j) >= floor_w)
+            take_if_better(best, gumbel_key(lj[j], inv_t, exp_noise_of(word_of(w, j))), i0 + j);
+}
+
 template <bool kPhilox>
-__global__ void __launch_bounds__(kThreads) sample_kernel(
+__global__ void __launch_bounds__(kThreads, 8) sample_kernel(
         const float* __restrict__ logits, const float* __restrict__ temperatures,
         const float* __restrict__ noise, uint64_t seed, uint64_t offset, int32_t num_rows,
         int32_t vocab, bool vec_ok, int32_t* __restrict__ out, uint32_t* status) {
@@ -161,11 +185,19 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
     __shared__ float warp_key[kThreads / 32];
     __shared__ int warp_idx[kThreads / 32];
     __shared__ Cand cta_best[2];          // by row parity: one cluster barrier per row
+    // in-kernel noise: the CTA's floor (an ordered int, see `ordered`) by row
+    // parity; the slot of the next row is reset during this one, after the
+    // last row that used it has passed its cluster barrier
+    __shared__ int cta_floor[2];
+    if (kPhilox && threadIdx.x < 2) cta_floor[threadIdx.x] = ordered(-CUDART_INF_F);
+    __syncthreads();
 
-    const PhiloxKeys keys = philox_keys(kPhilox ? seed : 0);
+    PhiloxKeys keys;
+    if constexpr (kPhilox) keys = philox_keys(seed);
     // persistent: a cluster per resident slot walks rows blockIdx.y, +gridDim.y, ...
     int par = 0;
     for (int64_t row = blockIdx.y; row < num_rows; row += gridDim.y, par ^= 1) {
+    if (kPhilox && threadIdx.x == 0) cta_floor[par ^ 1] = ordered(-CUDART_INF_F);
     const float temp = temperatures[row];
     const bool t_ok = isfinite(temp) && temp > 0.f;
     Cand best{-CUDART_INF_F, INT_MAX};
@@ -205,50 +237,47 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(
                 }
             }
             if constexpr (kPhilox) {
-                // warp-uniform trip count (the warp's best is a warp-wide
-                // reduction); lane l of warp w takes vectors 32w + l, + 256, ...
+                // One vector (4 entries) per lane and iteration: lane l of
+                // warp w takes vectors 32w + l, + 256, ...; the trip count is
+                // warp-uniform (the floor below is a warp-wide maximum).
+                // Entry lo + 4v has Philox counter n4 = base4 + v.  Few
+                // registers, so 8 CTAs fit per SM and their loads hide each
+                // other's latency.
+                //
+                // The floor T0 an entry must reach is a lower bound on the
+                // key of some entry that is (or will be) taken exactly: the
+                // CTA's floor so far (each warp publishes its own through
+                // shared memory), or x - kMinBonus for the largest scaled logit
+                // x of this lane's block (every key is at least x - ln(24 ln 2),
+                // as E <= 24 ln 2), lowered by margins for the float rounding
+                // of either.  The entry that gives a bound always reaches it,
+                // so it is taken.
                 const int lane = threadIdx.x & 31;
                 const float c1 = inv_t * kLog2e;
-                float wbest = -CUDART_INF_F;               // best key of the warp so far
-                int vb = threadIdx.x & ~31;
-                float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (vb + lane < nvec) l4 = pkv::ld_stream16f(lrow + lo + 4 * (vb + lane));
-                for (; vb < nvec; vb += kThreads) {
+                const uint64_t base4 = (n_row + (uint64_t)lo) >> 2;
+                float wfloor = -CUDART_INF_F;              // floor known to this warp
+                int k = 0;                                 // iterations done
+                for (int vb = threadIdx.x & ~31; vb < nvec; vb += kThreads, ++k) {
                     const int v = vb + lane;
                     const bool in = v < nvec;
-                    const int i = lo + 4 * v;
-                    // the next vector's logits in flight while this one is done
-                    const int vn = v + kThreads;
-                    float4 l4n = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (vn < nvec) l4n = pkv::ld_stream16f(lrow + lo + 4 * vn);
-                    const uint4 w = philox_block_keys((n_row + (uint64_t)i) >> 2, offset, keys);
-                    // T0 a little below the warp's best: the formula's own
-                    // rounding (about 1e-6 of the key) stays inside it
-                    const float t0 = wbest - (1e-3f + 1e-4f * fabsf(wbest));
-                    const float c0 = -t0 * kLog2e;
-                    const float lj[4] = {l4.x, l4.y, l4.z, l4.w};
-                    // one bound for the block, from its largest logit (NaN
-                    // entries are ignored by the max; a block of NaN passes)
-                    const float lmax = fmaxf(fmaxf(l4.x, l4.y), fmaxf(l4.z, l4.w));
-                    // nothing taken yet: every entry gets the exact key
-                    const uint32_t floor_w =
-                        best.idx == INT_MAX ? 0u : reach_floor(fmaf(lmax, c1, c0));
-                    uint32_t cand = 0;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) cand |= (uint32_t)(word_of(w, j) >= floor_w) << j;
-                    if (!in) cand = 0;
-                    // the exact keys, one passing entry at a time (a loop
-                    // with a data-dependent count, so the two logarithms are
-                    // branched over rather than predicated in every lane)
-                    while (cand) {
-                        const int j = __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        const float lv = j == 0 ? lj[0] : j == 1 ? lj[1] : j == 2 ? lj[2] : lj[3];
-                        take_if_better(best, gumbel_key(lv, inv_t, exp_noise_of(word_of(w, j))),
-                                       i + j);
+                    float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (in) l4 = pkv::ld_stream16f(lrow + lo + 4 * v);
+                    const uint4 w = philox_block_keys(base4 + (uint64_t)v, offset, keys);
+                    const float m = in ? max4(l4) : -CUDART_INF_F;
+                    const float x = m * inv_t;
+                    const float own = x - (kMinBonus + 1e-4f * fabsf(x));
+                    const float f = fmaxf(wfloor, own);         // NaN bounds are ignored
+                    const float t0 = f - (1e-3f + 1e-4f * fabsf(f));
+                    const uint32_t fw = reach_floor(fmaf(m, c1, -t0 * kLog2e));
+                    if (in && max4u(w) >= fw) exact_block(best, l4, w, fw, inv_t, lo + 4 * v);
+                    // a lane's own bound and best enter the floor at once;
+                    // the warp and the CTA exchange theirs every 4 iterations
+                    wfloor = fmaxf(wfloor, fmaxf(best.key, own));
+                    if ((k & 3) == 3) {
+                        const int wf = __reduce_max_sync(0xffffffffu, ordered(wfloor));
+                        if (lane == 0) atomicMax(&cta_floor[par], wf);
+                        wfloor = unordered(max(wf, *(volatile int*)&cta_floor[par]));
                     }
-                    wbest = unordered(__reduce_max_sync(0xffffffffu, ordered(best.key)));
-                    l4 = l4n;
                 }
             } else {
                 for (int v = v0; v < nvec; v += kThreads) {
@@ -364,25 +393,27 @@ int launch_sample(const float* logits, const float* temperatures, const float* e
         if (csize < 1) csize = 1;
     } else {
         // drawing it is arithmetic-bound, so a partial last wave of clusters
-        // costs time in proportion: take the cluster size c (at most 8, at
+        // costs time in proportion: take a cluster size c (at most 8, at
         // least 4096 entries per CTA) with the fewest waves of row segments,
-        // ceil(batch / resident clusters(c)) / c; ties go to the larger c
-        // (B=512 x V=151936: 8 CTAs per SM give 1216 CTA slots, and c = 7 runs
-        // 3 waves of 1/7 rows where c = 4 runs 2 of 1/4)
+        // ceil(batch / resident clusters(c)) / c, and among those the middle
+        // one: more CTAs per row pay more row ends (cluster barriers, start-up
+        // latency), fewer leave SMs unevenly loaded.  (B=512 x V=151936, 8 CTAs
+        // per SM: c = 2, 4 and 8 tie; measured 123, 113 and 132 us.)
         int c_max = (vocab + 4095) / 4096;
         if (c_max > 8) c_max = 8;
         if (c_max < 1) c_max = 1;
-        csize = 1;
+        int tied[8], n_tied = 0;
         double best = 1e30;
         for (int c = 1; c <= c_max; ++c) {
             const int n = resident_clusters<true>(c);
-            const double waves = (double)((batch + n - 1) / n);
-            const double cost = waves / c;
-            if (cost <= best * (1.0 + 1e-9)) {
+            const double cost = (double)((batch + n - 1) / n) / c;
+            if (cost < best * (1.0 - 1e-9)) {
                 best = cost;
-                csize = c;
+                n_tied = 0;
             }
+            if (cost <= best * (1.0 + 1e-9)) tied[n_tied++] = c;
         }
+        csize = tied[(n_tied - 1) / 2];
     }
     const int n_res = resident_clusters<kPhilox>(csize);
     const int32_t clusters = batch < n_res ? batch : n_res;

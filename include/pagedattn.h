@@ -282,7 +282,9 @@ PKV_API size_t pkv_paged_prefill_workspace_bytes(int32_t batch, int32_t total_q,
  *   workspace     device, >= pkv_paged_prefill_workspace_bytes(...) bytes,
  *                 16-byte aligned; holds the tile schedule
  * A sequence with inconsistent lengths sets PKV_STATUS_BAD_SEQLENS and is
- * skipped (its output rows are not written).  head_dim 64 or 128.
+ * skipped (its output rows are not written).  head_dim 64 or 128, any
+ * block_size.  PKV_ERR_UNSUPPORTED: num_blocks*block_size >= 2^31 (no such
+ * pool fits in device memory) or a driver without cuTensorMapEncodeTiled.
  */
 PKV_API int pkv_paged_prefill_varlen(const void* q, const void* k, const void* v,
                              const void* k_cache, const void* v_cache,

@@ -11,14 +11,10 @@
 // from the cache through block_tables[b], keys j >= c are rows of this call's
 // k / v.
 //
-// This file holds the tile scheduler shared by both prefill kernels, the
-// entry point, and the general kernel (any block size, head_dim 64 or 128):
-// FlashAttention-2-style tiles of 64 queries x 64 keys on mma.sync, four warps
-// of 16 query rows, K/V tiles gathered row by row through the block table with
-// cp.async into XOR-swizzled shared memory (double-buffered), ldmatrix
-// fragments, online softmax in registers.  The tcgen05/TMA kernel in
-// prefill_tc.cu takes over when the block size is a multiple of 128 and
-// head_dim is 128.
+// This file holds the tile scheduler (the plan kernel that lists the
+// (sequence, q tile) pairs of a call, longest first), the argument checks and
+// the entry points; the attention itself is the tcgen05 kernel of
+// prefill_tc.cu (head_dim 64 or 128, any block size).
 #include "prefill_common.cuh"
 
 using pkv::PrefillArgs;
@@ -146,277 +142,13 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(PrefillArgs 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// ---------------------------------------------------------------------------
-// general kernel (mma.sync)
-// ---------------------------------------------------------------------------
-constexpr int kBM = 64, kBN = 64, kThreadsG = 128;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-// 16-byte chunk cc of tile row r, XOR-swizzled so ldmatrix rows hit distinct banks
-template <int CH>
-__device__ __forceinline__ int swz(int r, int cc) {
-    return r * CH + (cc ^ (r & 7));
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreadsG) prefill_general_kernel(PrefillArgs a,
-                                                                    int32_t slot_base) {
-    constexpr int CH = D / 8;
-    extern __shared__ uint4 smem[];
-    uint4* sQ = smem;
-    uint4* sK = sQ + kBM * CH;
-    uint4* sV = sK + 2 * kBN * CH;
-
-    asm volatile("griddepcontrol.wait;" ::: "memory");    // the plan's tile list
-    const int h = blockIdx.x;
-    const int32_t slot = slot_base + (int32_t)blockIdx.y;
-    if (slot >= a.sched[0]) return;
-    const int2 tile = a.tiles[slot];
-    const int32_t b = tile.x, m = tile.y;
-    int32_t q0, lq, lk;
-    pkv::seq_lengths(a, b, q0, lq, lk, false);
-    const int32_t c = lk - lq;
-    const int32_t kvh = h / a.G;
-    const int32_t row0 = m * kBM;
-    const int32_t rows = min(kBM, lq - row0);
-    const int32_t kv_limit = min(lk, c + row0 + kBM);
-    const int32_t n_tiles = (kv_limit + kBN - 1) / kBN;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int32_t* bt_row = a.bt ? a.bt + (int64_t)b * a.MB : nullptr;
-
-    // ---- Q tile ----
-    for (int idx = tid; idx < kBM * CH; idx += kThreadsG) {
-        const int r = idx / CH, cc = idx - r * CH;
-        const bool ok = r < rows;
-        const __nv_bfloat16* src =
-            ok ? a.q + ((int64_t)(q0 + row0 + r) * a.Hq + h) * D + cc * 8 : a.q;
-        cp_async16(smem_u32(sQ + swz<CH>(r, cc)), src, ok ? 16 : 0);
-    }
-    cp_async_commit();
-
-    bool bad_block = false;
-    auto load_kv = [&](int n, int st) {
-        uint4* dk = sK + st * kBN * CH;
-        uint4* dv = sV + st * kBN * CH;
-        for (int idx = tid; idx < kBN * CH; idx += kThreadsG) {
-            const int r = idx / CH, cc = idx - r * CH;
-            const int32_t j = n * kBN + r;
-            const __nv_bfloat16* ks = nullptr;
-            const __nv_bfloat16* vs = nullptr;
-            if (j < kv_limit) {
-                if (j < c) {
-                    const int32_t blk = bt_row[j / a.bs];
-                    if ((unsigned)blk < (unsigned)a.NB) {
-                        const int64_t off =
-                            (((int64_t)blk * a.bs + j % a.bs) * a.Hkv + kvh) * D + cc * 8;
-                        ks = a.kc + off;
-                        vs = a.vc + off;
-                    } else {
-                        bad_block = true;
-                    }
-                } else {
-                    const int64_t off = ((int64_t)(q0 + j - c) * a.Hkv + kvh) * D + cc * 8;
-                    ks = a.k + off;
-                    vs = a.v + off;
-                }
-            }
-            cp_async16(smem_u32(dk + swz<CH>(r, cc)), ks ? ks : a.k, ks ? 16 : 0);
-            cp_async16(smem_u32(dv + swz<CH>(r, cc)), vs ? vs : a.v, vs ? 16 : 0);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-
-    // ---- Q fragments ----
-    uint32_t qf[D / 16][4];
-    {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int r = warp * 16 + (mi & 1) * 8 + rr;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            ldsm_x4(smem_u32(sQ + swz<CH>(r, 2 * kk + (mi >> 1))), qf[kk][0], qf[kk][1],
-                    qf[kk][2], qf[kk][3]);
-    }
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_i[2] = {-INFINITY, -INFINITY}, l_i[2] = {0.f, 0.f};
-    const int32_t pos_lo = c + row0 + warp * 16 + g;     // query positions of rows g, g+8
-    const int32_t pos_hi = pos_lo + 8;
-
-    for (int n = 0; n < n_tiles; ++n) {
-        if (n + 1 < n_tiles) {
-            load_kv(n + 1, (n + 1) & 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const uint4* tk = sK + (n & 1) * kBN * CH;
-        const uint4* tv = sV + (n & 1) * kBN * CH;
-        float s[kBN / 8][4];
-#pragma unroll
-        for (int i = 0; i < kBN / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-        {
-            const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                for (int np = 0; np < kBN / 16; ++np) {
-                    const int r = np * 16 + (mi >> 1) * 8 + rr;
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(tk + swz<CH>(r, 2 * kk + (mi & 1))), b0, b1, b2, b3);
-                    pkv::mma_bf16_16816(s[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
-                                        b0, b1);
-                    pkv::mma_bf16_16816(s[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2],
-                                        qf[kk][3], b2, b3);
-                }
-            }
-        }
-        // ---- mask, online softmax (base 2) ----
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < kBN / 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int32_t j = n * kBN + nt * 8 + 2 * t + (e & 1);
-                const int32_t p = (e < 2) ? pos_lo : pos_hi;
-                const float x = (j <= p && j < lk) ? s[nt][e] * a.scale_log2 : -INFINITY;
-                s[nt][e] = x;
-                mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
-        }
-        float alpha[2], muse[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            const float mn = fmaxf(m_i[r], mx[r]);
-            muse[r] = (mn == -INFINITY) ? 0.f : mn;
-            alpha[r] = (m_i[r] == -INFINITY) ? 0.f : pkv::fast_exp2(m_i[r] - muse[r]);
-            m_i[r] = mn;
-            l_i[r] *= alpha[r];
-        }
-#pragma unroll
-        for (int nt = 0; nt < kBN / 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p = pkv::fast_exp2(s[nt][e] - muse[e >> 1]);
-                s[nt][e] = p;
-                l_i[e >> 1] += p;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= alpha[0]; o[i][1] *= alpha[0];
-            o[i][2] *= alpha[1]; o[i][3] *= alpha[1];
-        }
-        // ---- O += P V ----
-        {
-            const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int kc = 0; kc < kBN / 16; ++kc) {
-                const uint32_t a0 = pkv::pack_bf16(s[2 * kc][0], s[2 * kc][1]);
-                const uint32_t a1 = pkv::pack_bf16(s[2 * kc][2], s[2 * kc][3]);
-                const uint32_t a2 = pkv::pack_bf16(s[2 * kc + 1][0], s[2 * kc + 1][1]);
-                const uint32_t a3 = pkv::pack_bf16(s[2 * kc + 1][2], s[2 * kc + 1][3]);
-                const int r = kc * 16 + (mi & 1) * 8 + rr;
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(tv + swz<CH>(r, 2 * dp + (mi >> 1))), b0, b1, b2, b3);
-                    pkv::mma_bf16_16816(o[2 * dp], a0, a1, a2, a3, b0, b1);
-                    pkv::mma_bf16_16816(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-        }
-        __syncthreads();
-    }
-    if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
-    // ---- epilogue ----
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l_i[r] += __shfl_xor_sync(0xffffffffu, l_i[r], 1);
-        l_i[r] += __shfl_xor_sync(0xffffffffu, l_i[r], 2);
-        l_i[r] = l_i[r] > 0.f ? 1.f / l_i[r] : 0.f;
-    }
-    const int r_lo = warp * 16 + g, r_hi = r_lo + 8;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const int d = i * 8 + 2 * t;
-        if (r_lo < rows)
-            *reinterpret_cast<uint32_t*>(a.out + ((int64_t)(q0 + row0 + r_lo) * a.Hq + h) * D +
-                                         d) = pkv::pack_bf16(o[i][0] * l_i[0], o[i][1] * l_i[0]);
-        if (r_hi < rows)
-            *reinterpret_cast<uint32_t*>(a.out + ((int64_t)(q0 + row0 + r_hi) * a.Hq + h) * D +
-                                         d) = pkv::pack_bf16(o[i][2] * l_i[1], o[i][3] * l_i[1]);
-    }
-}
-
-template <int D>
-int launch_general(PrefillArgs& a, cudaStream_t s, const PrefillPrologue* pre) {
-    const size_t smem = (size_t)(kBM + 4 * kBN) * (D / 8) * 16;
-    static std::atomic<uint64_t> configured{0};
-    if (!pkv_dynamic_smem_once((const void*)prefill_general_kernel<D>, (int)smem, configured))
-        return PKV_ERR_CUDA;
-    a.tile_m = kBM;
-    a.tile_n = kBN;
-    const int rc = pkv_launch_prefill_plan(a, s, pre);
-    if (rc != PKV_OK) return rc;
-    for (int32_t base = 0; base < a.max_tiles; base += 65535) {
-        const int32_t n = a.max_tiles - base < 65535 ? a.max_tiles - base : 65535;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)a.Hq, (unsigned)n, 1);
-        cfg.blockDim = dim3(kThreadsG, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = s;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, prefill_general_kernel<D>, a, base) != cudaSuccess)
-            return PKV_ERR_CUDA;
-    }
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
-}
-
 }  // namespace
 
 PrefillLayout pkv_prefill_layout(int32_t batch, int32_t total_q) {
     PrefillLayout L{};
-    // the smallest q tile of either kernel (64) bounds the tile count
-    L.max_tiles = (int32_t)(((int64_t)total_q + kBM - 1) / kBM + batch);
+    // sequence b has ceil(lq_b / 128) q tiles <= lq_b / 128 + 1
+    L.max_tiles = (int32_t)(((int64_t)total_q + pkv::kPrefillTileQ - 1) / pkv::kPrefillTileQ +
+                            batch);
     L.off_sched = 0;
     L.off_tiles = 256;
     L.total = (L.off_tiles + sizeof(int2) * (size_t)L.max_tiles + 255) & ~(size_t)255;
@@ -446,15 +178,12 @@ int pkv_launch_prefill_plan(PrefillArgs& a, cudaStream_t s, const PrefillPrologu
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// tcgen05 fast path (prefill_tc.cu): returns PKV_ERR_UNSUPPORTED when the
-// shapes are not its own.
+// The tcgen05 kernel (prefill_tc.cu).  PKV_ERR_UNSUPPORTED: head_dim other
+// than 64 / 128, a pool of 2^31 rows or more, or no tensor-map encoder in the
+// driver.
 int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim);
 int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
                          const PrefillPrologue* pre);
-
-namespace {
-
-}  // namespace
 
 // Checks every argument and fills the kernel arguments; enqueues nothing.
 int pkv_prefill_make_args(const void* q, const void* k, const void* v, const void* k_cache,
@@ -515,9 +244,9 @@ int pkv_prefill_make_args(const void* q, const void* k, const void* v, const voi
 }
 
 int pkv_prefill_launch(PrefillArgs& a, int head_dim, cudaStream_t s, const PrefillPrologue* pre) {
-    if (pkv_prefill_tc_supported(a, head_dim) == PKV_OK)
-        return pkv_launch_prefill_tc(a, head_dim, s, pre);
-    return head_dim == 128 ? launch_general<128>(a, s, pre) : launch_general<64>(a, s, pre);
+    const int rc = pkv_prefill_tc_supported(a, head_dim);
+    if (rc != PKV_OK) return rc;
+    return pkv_launch_prefill_tc(a, head_dim, s, pre);
 }
 
 int pkv_enqueue_store(void* ctx, bool* launched) {

@@ -5,6 +5,9 @@
 
 namespace pkv {
 
+constexpr int kPrefillTileQ = 128;    // queries per tile of the prefill kernel
+constexpr int kPrefillTileK = 128;    // keys per tile
+
 struct PrefillArgs {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;

@@ -1,6 +1,7 @@
 // paged_prefill_varlen on the 5th-generation tensor cores: tcgen05.mma with
-// TMEM accumulators, Q/K/V tiles staged by TMA, for head_dim 128 or 64 and
-// block sizes that are multiples of 128 or one of 8, 16, 32, 64.
+// TMEM accumulators, Q/K/V tiles staged by TMA (or gathered row by row with
+// cp.async for block sizes TMA boxes cannot tile), for head_dim 128 or 64 and
+// any block size.
 //
 // What it computes is stated in prefill.cu (causal varlen prefill over a
 // prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
@@ -14,14 +15,17 @@
 //     prefix, per half of head_dim one TMA box at row
 //     block_tables[b][128u / bs] * bs + (128u % bs) of the pool when bs is a
 //     multiple of 128, else 128/bs boxes of bs rows, one per block, stacked
-//     in shared memory (keys past the prefix read zeros);
+//     in shared memory, when bs is 8, 16, 32 or 64; for other block sizes
+//     (below 8, or not dividing 128) the producer warp gathers the tile's
+//     rows with 16-byte cp.async copies into the same swizzled layout (keys
+//     past the prefix read zeros either way);
 //   * new tiles t = 0 .. m: the chunk's own k/v rows q0 + 128t ..; tile t == m
 //     is the diagonal (causal mask col <= row), tiles t > m are never visible.
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
 // shared memory because unused cache slots may hold NaN.
 //
 // Roles (256 threads, one CTA per SM; 224 without warp 7 when cached tiles
-// are gathered per block):
+// are loaded per block or gathered):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks (diagonal and partial tiles only) and stores
 //              P = exp2(S - m) as packed bf16 back into the first 64 columns of
@@ -70,21 +74,25 @@ using namespace pkv::tc;
 
 namespace {
 
-constexpr int kBM = 128;                 // queries per tile
-constexpr int kBN = 128;                 // keys per tile
+constexpr int kBM = pkv::kPrefillTileQ;  // queries per tile
+constexpr int kBN = pkv::kPrefillTileK;  // keys per tile
 // head_dim D is 128 or 64: a tile is D/64 column blocks of 64 bf16 (one
 // 128-byte swizzle atom wide), each 128 rows x 128 B
 constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
-constexpr int kThreads = 256;            // 224 (no V producer warp) with kBoxed
+constexpr int kThreads = 256;            // 224 (no V producer warp) unless kLoadTile
+// How a cached 128-key tile reaches shared memory, by block size: one TMA box
+// (a multiple of 128), one TMA box per block (8, 16, 32, 64), or rows gathered
+// by the producer warp with cp.async (any other block size).
+constexpr int kLoadTile = 0, kLoadBoxes = 1, kLoadGather = 2;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
 constexpr int kItemReaders = 7;          // V producer, Q K^T and P V issuers, 4 softmax warps
-// With kBoxed the K producer also loads V (a second thread gathering the same
-// boxes measured 10-14% slower), so the V producer warp is not launched.
-template <bool kBoxed>
-constexpr int threads_for() { return kBoxed ? kThreads - 32 : kThreads; }
-template <bool kBoxed>
-constexpr int item_readers_for() { return kBoxed ? kItemReaders - 1 : kItemReaders; }
+// Unless kLoadTile the K producer also loads V (a second thread gathering the
+// same boxes measured 10-14% slower), so the V producer warp is not launched.
+template <int kLoad>
+constexpr int threads_for() { return kLoad != kLoadTile ? kThreads - 32 : kThreads; }
+template <int kLoad>
+constexpr int item_readers_for() { return kLoad != kLoadTile ? kItemReaders - 1 : kItemReaders; }
 constexpr uint32_t kColS0 = 0, kColO = 384;
 constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
@@ -263,15 +271,66 @@ __device__ __forceinline__ void load_tile(unsigned char* dst, const CUtensorMap*
     }
 }
 
-// kBoxed: the pool's blocks hold fewer than 128 keys, so a cached tile is
-// gathered from 128/bs boxes (a separate instantiation keeps the common
-// one-box producer loop free of that code).  kPolls: the waits take their
+// 16 bytes global -> shared with cp.async; `bytes` 0 writes zeros and reads
+// nothing.
+__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr(smem)), "l"(gmem),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+// Gathers cached tile j of item x (keys 128j .. 128j+127 of the prefix) into
+// a K and a V stage: lane l copies rows l, l+32, l+64, l+96, each 16-byte
+// chunk c of a row to where a 128-byte-swizzled TMA box would put it (64-column
+// block c/8, row r, chunk (c%8) ^ (r%8)).  Keys past the prefix or in a block
+// outside the pool read zeros; the latter set `bad`.
+template <int D>
+__device__ __forceinline__ void gather_cached_tile(const PrefillArgs& a, const Item& x, int32_t j,
+                                                   int32_t kvh, unsigned char* kdst,
+                                                   unsigned char* vdst, int lane, bool& bad) {
+#pragma unroll
+    for (int rr = 0; rr < kBN / 32; ++rr) {
+        const int r = lane + 32 * rr;
+        const int32_t key = j * kBN + r;
+        int32_t blk = -1;
+        if (key < x.c) {
+            blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
+            if ((unsigned)blk >= (unsigned)a.NB) {
+                bad = true;
+                blk = -1;
+            }
+        }
+        const uint32_t bytes = blk >= 0 ? 16u : 0u;
+        const int64_t src_row = blk >= 0 ? (int64_t)blk * a.bs + key % a.bs : 0;
+        const __nv_bfloat16* ksrc = a.kc + (src_row * a.Hkv + kvh) * D;
+        const __nv_bfloat16* vsrc = a.vc + (src_row * a.Hkv + kvh) * D;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const int off = (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+            cp_async16_zfill(kdst + off, ksrc + c * 8, bytes);
+            cp_async16_zfill(vdst + off, vsrc + c * 8, bytes);
+        }
+    }
+}
+
+// kLoad: how cached tiles are loaded (see kLoadTile); the two per-block
+// modes are instantiations of their own so the common one-box producer loop
+// carries none of their code.  kPolls: the waits take their
 // poll limit from the arguments (pkv_set_wait_poll_limit) instead of the
 // compile-time default, in instantiations of their own (a run-time limit in
 // the tight waits of the issuers cost the default kernel about 5%).
-template <int D, bool kBoxed, bool kPolls>
+template <int D, int kLoad, bool kPolls>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
+    constexpr bool kBoxed = kLoad == kLoadBoxes;
+    constexpr bool kGather = kLoad == kLoadGather;
     const uint32_t polls = kPolls ? a.wait_polls : (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     constexpr int kTile = TcSmem<D>::kTile;
     constexpr int kBlocks = D / 64;               // 64-column blocks of a tile
@@ -296,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         mbar_init(&s.o_free, 128);
         for (int q = 0; q < kItemRing; ++q) {
             mbar_init(&s.item_full[q], 1);
-            mbar_init(&s.item_empty[q], item_readers_for<kBoxed>());
+            mbar_init(&s.item_empty[q], item_readers_for<kLoad>());
         }
         mbar_init(&s.mma_done, 2);
         mbar_init_fence();
@@ -312,7 +371,102 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     // if any role gave up: tiles into the ring, and Q tiles
     uint32_t tiles_issued = 0, q_issued = 0;
 
-    if (warp == 4) {
+    if (kGather && warp == 4) {
+        // ------------------------------------------------------ gather producer
+        // The whole warp: lane 0 claims items, loads Q and the chunk's own K/V
+        // tiles by TMA; every lane gathers cached tiles with cp.async, one
+        // commit group per tile.  A gathered tile's K and V barriers are
+        // arrived once its group has landed (wait_group, then a proxy fence so
+        // the tensor core sees the writes, then lane 0 arrives), one tile
+        // behind the copies being issued so two tiles are in flight.
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.v);
+        }
+        uint32_t& T = tiles_issued;               // tiles whose barriers will complete
+        uint32_t I = 0;
+        bool ok = true, bad_block = false;
+        int pend = -1;                            // stage of a gathered tile in flight
+        auto land = [&](int st_) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s.k_full[st_]);
+                mbar_arrive(&s.v_full[st_]);
+            }
+        };
+        for (; ok; ++I) {
+            const int qs = I % kItemRing;
+            if (I >= kItemRing && !(ok = warp_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1,
+                                                   &s.abort_flag, polls)))
+                break;
+            int32_t it = 0;
+            if (lane == 0) {
+                it = atomicAdd(&a.sched[1], 1);
+                s.item_ring[qs] = it < n_items ? it : -1;
+                mbar_arrive(&s.item_full[qs]);
+            }
+            it = __shfl_sync(0xffffffffu, it, 0);
+            if (it >= n_items) break;
+            const Item x = item_at(a, it);
+            const int32_t kvh = x.h / a.G;
+            if (I > 0 && !(ok = warp_wait(&s.q_free, (I - 1) & 1, &s.abort_flag, polls))) break;
+            if (lane == 0) {
+                mbar_expect_tx(&s.q_full, kTile);
+                for (int hf = 0; hf < kBlocks; ++hf)
+                    tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
+                                x.q0 + x.m * kBM);
+            }
+            ++q_issued;
+            for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
+                const int st = T % kStages;
+                const uint32_t use = T / kStages;
+                if (use > 0 && !(ok = warp_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_flag,
+                                                polls)))
+                    break;
+                if (use > 0 && !(ok = warp_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag,
+                                                polls)))
+                    break;
+                if (j < x.n_cached) {
+                    gather_cached_tile<D>(a, x, j, kvh, s.k[st], s.v[st], lane, bad_block);
+                    cp_async_commit();
+                    if (pend >= 0) {
+                        cp_async_wait<1>();          // the tile before this one has landed
+                        land(pend);
+                    }
+                    pend = st;
+                } else {
+                    // cached tiles come first in an item: the last one lands now
+                    if (pend >= 0) {
+                        cp_async_wait<0>();
+                        land(pend);
+                        pend = -1;
+                    }
+                    if (lane == 0) {
+                        const int32_t row = x.q0 + (j - x.n_cached) * kBN;
+                        mbar_expect_tx(&s.k_full[st], kTile);
+                        for (int hf = 0; hf < kBlocks; ++hf)
+                            tma_load_3d(s.k[st] + hf * kHalf, &maps.k, &s.k_full[st], hf * 64,
+                                        kvh, row);
+                        mbar_expect_tx(&s.v_full[st], kTile);
+                        for (int hf = 0; hf < kBlocks; ++hf)
+                            tma_load_3d(s.v[st] + hf * kHalf, &maps.v, &s.v_full[st], hf * 64,
+                                        kvh, row);
+                    }
+                }
+            }
+        }
+        // copies still in flight land, and complete their barriers, before
+        // anything else (on every way out)
+        if (pend >= 0) {
+            cp_async_wait<0>();
+            land(pend);
+        }
+        if (__any_sync(0xffffffffu, bad_block) && lane == 0)
+            pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
+        if (!ok && lane == 0) give_up(s, a.status);
+    } else if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&maps.q);
@@ -357,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     mbar_expect_tx(&s.k_full[st], kTile);
                     load_tile<D, kBoxed>(s.k[st], cached ? &maps.kc : &maps.k, &s.k_full[st], kvh,
                                          cached, row, rows, a.bs);
-                    if constexpr (kBoxed) {
+                    if constexpr (kLoad != kLoadTile) {
                         if (use > 0 &&
                             !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
                                     &s.abort_flag, polls))) {
@@ -373,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
             if (!ok) give_up(s, a.status);
         }
-    } else if (!kBoxed && warp == 7) {
+    } else if (kLoad == kLoadTile && warp == 7) {
         // ------------------------------------------------------------ V producer
         // V tiles on their own thread: a V stage waits for its P V, and in
         // the producer's loop that wait held back the next K tile
@@ -664,14 +818,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (s.abort_flag && lane == 0 && (warp == 4 || (!kBoxed && warp == 7))) {
+    if (s.abort_flag && lane == 0 && (warp == 4 || (kLoad == kLoadTile && warp == 7))) {
         // some role gave up: every copy this producer issued lands before the
         // CTA exits (a consumer may have given up after the last one was issued)
         const bool k_side = warp == 4;
         for (uint32_t back = 1; back <= (uint32_t)kStages && back <= tiles_issued; ++back) {
             const uint32_t t = tiles_issued - back;
             if (k_side) mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
-            if (!k_side || kBoxed) mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
+            if (!k_side || kLoad != kLoadTile)
+                mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
         }
         if (k_side && q_issued > 0) mbar_drain(&s.q_full, (q_issued - 1) & 1);
     }
@@ -685,16 +840,26 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int 
     return pkv::tma_encode_rows(m, base, rows, heads, head_dim, box_rows);
 }
 
+// The load mode of a call's cached tiles (see kLoadTile).
+int load_mode(const PrefillArgs& a) {
+    if (a.bt == nullptr || a.bs % kBN == 0) return kLoadTile;
+    if (a.bs % 8 == 0 && kBN % a.bs == 0) return kLoadBoxes;
+    return kLoadGather;
+}
+
 template <int D>
 int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillPrologue* pre) {
+    using Kernel = void (*)(const TcMaps, const PrefillArgs);
+    static const Kernel kernels[3][2] = {
+        {prefill_tc_kernel<D, kLoadTile, false>, prefill_tc_kernel<D, kLoadTile, true>},
+        {prefill_tc_kernel<D, kLoadBoxes, false>, prefill_tc_kernel<D, kLoadBoxes, true>},
+        {prefill_tc_kernel<D, kLoadGather, false>, prefill_tc_kernel<D, kLoadGather, true>}};
     const int smem = (int)sizeof(TcSmem<D>) + 1024;
-    const bool boxed = a.bt != nullptr && a.bs % kBN != 0;
-    const bool custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS;
-    void (*kernel)(const TcMaps, const PrefillArgs) =
-        boxed ? (custom ? prefill_tc_kernel<D, true, true> : prefill_tc_kernel<D, true, false>)
-              : (custom ? prefill_tc_kernel<D, false, true> : prefill_tc_kernel<D, false, false>);
-    static std::atomic<uint64_t> configured[4];
-    if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[(boxed ? 2 : 0) + custom]))
+    const int mode = load_mode(a);
+    const int custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS ? 1 : 0;
+    const Kernel kernel = kernels[mode][custom];
+    static std::atomic<uint64_t> configured[6];
+    if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[mode * 2 + custom]))
         return PKV_ERR_CUDA;
     a.tile_m = kBM;
     a.tile_n = kBN;
@@ -709,7 +874,8 @@ int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(boxed ? threads_for<true>() : threads_for<false>(), 1, 1);
+    cfg.blockDim = dim3(mode == kLoadTile ? threads_for<kLoadTile>() : threads_for<kLoadBoxes>(),
+                        1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -722,8 +888,6 @@ int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillP
 
 int pkv_prefill_tc_supported(const PrefillArgs& a, int head_dim) {
     if (head_dim != 128 && head_dim != 64) return PKV_ERR_UNSUPPORTED;
-    if (a.bt != nullptr && a.bs % kBN != 0 && (a.bs % 8 != 0 || kBN % a.bs != 0))
-        return PKV_ERR_UNSUPPORTED;
     if ((int64_t)a.NB * a.bs >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
     if (pkv::tma_encode_fn() == nullptr) return PKV_ERR_UNSUPPORTED;
     return PKV_OK;
@@ -736,7 +900,7 @@ int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
         !encode_rows(&maps.k, a.k, a.total_q, a.Hkv, head_dim) ||
         !encode_rows(&maps.v, a.v, a.total_q, a.Hkv, head_dim))
         return PKV_ERR_CUDA;
-    if (a.bt) {
+    if (a.bt && load_mode(a) != kLoadGather) {
         const int box = a.bs % kBN == 0 ? kBN : a.bs;
         if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, box) ||
             !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, box))

@@ -50,7 +50,7 @@ def test_workspace_queries_are_pure(lib):
     assert a == lib.pkv_paged_decode_workspace_bytes(64, 16, 4096, c) and a > 0
     assert lib.pkv_paged_decode_workspace_bytes(64, 16, 8192, c) >= a
     p = lib.pkv_paged_prefill_workspace_bytes(16, 16384, 32, c)
-    assert p >= 8 * (16384 // 64 + 16)
+    assert p >= 8 * (16384 // 128 + 16)       # one (sequence, 128-query tile) pair each
     # the mixed-batch call holds the prefill's schedule and a decode plan
     m = lib.pkv_paged_attention_varlen_workspace_bytes(16, 16384, 32, 8192, c)
     assert m >= p + lib.pkv_paged_decode_workspace_bytes(16, 32, 8192, c)

@@ -3,9 +3,10 @@
 
 pkv_kv_store_paged_prefill_varlen must leave the cache exactly as pkv_kv_store
 leaves it and give exactly the output of pkv_paged_prefill_varlen (same
-kernels, chained launches), on the tcgen05 path (head_dim 128, block size a
-multiple of 128) and on the general path, eagerly and replayed from a CUDA
-graph; its output also matches the float64 oracle."""
+kernels, chained launches), with each way the tcgen05 kernel loads cached
+tiles (one TMA box per tile for block sizes that are multiples of 128, one box
+per block for 8..64, rows gathered with cp.async for 4 and 48), eagerly and
+replayed from a CUDA graph; its output also matches the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +17,8 @@ from test_gpu_prefill import make_case
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(8, 2, 128, 256), (8, 2, 128, 128), (4, 1, 64, 16), (6, 3, 128, 32)]
+SHAPES = [(8, 2, 128, 256), (8, 2, 128, 128), (4, 1, 64, 16), (6, 3, 128, 32), (4, 2, 128, 4),
+          (8, 2, 64, 48)]
 
 
 def _slots(c, lens, cached, bs):
@@ -67,7 +69,7 @@ def test_fused_prefill_equals_store_then_prefill(cuda, hq, hkv, d, bs):
     assert torch.equal(flat_k[sl.long()], k)
 
 
-@pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 256), (4, 1, 64, 16)])
+@pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 256), (4, 1, 64, 16), (4, 2, 128, 48)])
 def test_fused_prefill_in_a_cuda_graph(cuda, hq, hkv, d, bs):
     pkv = U.lib()
     lens = [128, 77, 1, 256]

@@ -23,8 +23,8 @@ from test_gpu_prefill import make_case
 pytestmark = pytest.mark.gpu
 
 # (Hq, Hkv, D, block size): TMA decode + tcgen05 prefill; register decode +
-# boxed tcgen05 prefill; head_dim 64 on both TMA paths; register decode +
-# general prefill
+# tcgen05 prefill with a box per block; head_dim 64 on both TMA paths;
+# register decode + tcgen05 prefill with gathered cached rows
 SHAPES = [(8, 2, 128, 256), (8, 2, 128, 16), (4, 1, 64, 64), (6, 3, 128, 48)]
 
 

@@ -72,8 +72,9 @@ def test_tiny_with_and_without_block_tables(cuda):
     assert torch.equal(outs[0], outs[1])
 
 
-# head_dim 128 or 64 with block sizes 8..64 or multiples of 128 runs the tcgen05 kernel
-# (several TMA boxes per 128-key tile below 128); the others run the general kernel
+# the tcgen05 kernel's three ways of loading a cached 128-key tile: one TMA box
+# (block sizes that are multiples of 128), one box per block (8, 16, 32, 64), or
+# rows gathered by the producer warp with cp.async (4, 48)
 @pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 16), (4, 1, 64, 4), (6, 3, 128, 256),
                                          (2, 2, 64, 256), (16, 4, 128, 128), (8, 2, 128, 8),
                                          (4, 4, 128, 32), (8, 1, 128, 64), (4, 2, 128, 48),

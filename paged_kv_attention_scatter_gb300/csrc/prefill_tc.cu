@@ -1,7 +1,7 @@
 // paged_prefill_varlen on the 5th-generation tensor cores: tcgen05.mma with
-// TMEM accumulators, Q/K/V tiles staged by TMA (or gathered row by row with
-// cp.async for block sizes TMA boxes cannot tile), for head_dim 128 or 64 and
-// any block size.
+// TMEM accumulators, Q/K/V tiles staged by TMA (cached tiles gathered row by
+// row with cp.async when the block size is not a multiple of 128), for
+// head_dim 128 or 64 and any block size.
 //
 // What it computes is stated in prefill.cu (causal varlen prefill over a
 // prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
@@ -14,18 +14,17 @@
 //   * cached tiles u = 0 .. ceil(c/128)-1: keys 128u .. 128u+127 of the
 //     prefix, per half of head_dim one TMA box at row
 //     block_tables[b][128u / bs] * bs + (128u % bs) of the pool when bs is a
-//     multiple of 128, else 128/bs boxes of bs rows, one per block, stacked
-//     in shared memory, when bs is 8, 16, 32 or 64; for other block sizes
-//     (below 8, or not dividing 128) the producer warp gathers the tile's
-//     rows with 16-byte cp.async copies into the same swizzled layout (keys
-//     past the prefix read zeros either way);
+//     multiple of 128; for any other block size the producer warps gather the
+//     tile's rows with 16-byte cp.async copies into the same swizzled layout
+//     (keys past the prefix read zeros either way).  Per-block TMA boxes
+//     (8..64 rows, stacked) measured slower than the gather at every such
+//     block size, and a box below 8 rows would start inside a swizzle atom;
 //   * new tiles t = 0 .. m: the chunk's own k/v rows q0 + 128t ..; tile t == m
 //     is the diagonal (causal mask col <= row), tiles t > m are never visible.
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
 // shared memory because unused cache slots may hold NaN.
 //
-// Roles (256 threads, one CTA per SM; 224 without warp 7 when cached tiles
-// are loaded per block or gathered):
+// Roles (256 threads, one CTA per SM):
 //   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  It loads S,
 //              masks (diagonal and partial tiles only) and stores
 //              P = exp2(S - m) as packed bf16 back into the first 64 columns of
@@ -40,9 +39,9 @@
 //   warp 4     TMA producer (one thread): Q once per item, K tiles into a
 //              three-stage ring, a stage refilled as soon as its Q K^T is done.
 //   warp 7     TMA producer of the V tiles (one thread, three stages), a stage
-//              refilled once its P V is done; on its own thread so that wait
-//              never holds back a K tile.  With per-block boxes warp 4 loads V
-//              too (a second thread walking the same block table was slower).
+//              refilled once its P V is done; on its own warp so that wait
+//              never holds back a K tile.  When cached tiles are gathered,
+//              all 32 lanes of warps 4 and 7 take part (K and V respectively).
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for
@@ -79,22 +78,15 @@ constexpr int kBN = pkv::kPrefillTileK;  // keys per tile
 // head_dim D is 128 or 64: a tile is D/64 column blocks of 64 bf16 (one
 // 128-byte swizzle atom wide), each 128 rows x 128 B
 constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
-constexpr int kThreads = 256;            // 224 (no V producer warp) unless kLoadTile
+constexpr int kThreads = 256;
 // How a cached 128-key tile reaches shared memory, by block size: one TMA box
-// (a multiple of 128), one TMA box per block (8, 16, 32, 64), or rows gathered
-// by the producer warp with cp.async (any other block size).
-constexpr int kLoadTile = 0, kLoadBoxes = 1, kLoadGather = 2;
+// per 64-column block (a multiple of 128), or rows gathered by the producer
+// warps with cp.async (any other block size).
+constexpr int kLoadTile = 0, kLoadGather = 1;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
 constexpr int kItemReaders = 7;          // V producer, Q K^T and P V issuers, 4 softmax warps
-// Unless kLoadTile the K producer also loads V (a second thread gathering the
-// same boxes measured 10-14% slower), so the V producer warp is not launched.
-template <int kLoad>
-constexpr int threads_for() { return kLoad != kLoadTile ? kThreads - 32 : kThreads; }
-template <int kLoad>
-constexpr int item_readers_for() { return kLoad != kLoadTile ? kItemReaders - 1 : kItemReaders; }
 constexpr uint32_t kColS0 = 0, kColO = 384;
-constexpr int kMaxBoxes = kBN / 8;       // cache boxes per 128-key tile (block size >= 8)
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the tolerated growth
 // A tile computed against the running maximum is redone (maximum taken, O and
 // l rescaled) when its row sum of P passes 2^16, i.e. when some exponent may
@@ -213,62 +205,33 @@ __device__ __forceinline__ void give_up(Smem& s, uint32_t* status) {
     pkv::report(status, PKV_STATUS_WAIT_TIMEOUT);
 }
 
-// Where tile j of item x comes from: the chunk's own rows (map k/v, one box at
-// `row`), or the cache through the block table (one box at `row`, or with
-// kBoxed one box per block at rows[]; keys past the prefix or the pool read
-// zeros).  Returns whether it is a cached tile; sets `bad` on a block id
-// outside the pool.
-template <bool kBoxed>
+// Where tile j of item x comes from (one TMA box per 64-column block at
+// `row`): the chunk's own rows of k/v, or the pool row of key 128j through
+// the block table (keys past the prefix, or a block id outside the pool, read
+// the zeros TMA fills past the pool; the latter sets `bad`).  Returns whether
+// it is a cached tile.
 __device__ __forceinline__ bool tile_source(const PrefillArgs& a, const Item& x, int32_t j,
-                                            int32_t& row, int32_t* rows, bool& bad) {
-    const int32_t oob_row = a.NB * a.bs;   // past the pool: TMA fills zeros
-    row = oob_row;
+                                            int32_t& row, bool& bad) {
     if (j >= x.n_cached) {
         row = x.q0 + (j - x.n_cached) * kBN;
         return false;
     }
     const int32_t key0 = j * kBN;
-    if (!kBoxed) {
-        const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
-        if ((unsigned)blk < (unsigned)a.NB)
-            row = blk * a.bs + key0 % a.bs;
-        else
-            bad = true;
-    } else {
-#pragma unroll
-        for (int u = 0; u < kMaxBoxes; ++u) {
-            rows[u] = oob_row;
-            const int32_t key = key0 + u * a.bs;
-            if (key < key0 + kBN && key < x.c) {
-                const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
-                if ((unsigned)blk < (unsigned)a.NB)
-                    rows[u] = blk * a.bs + key % a.bs;
-                else
-                    bad = true;
-            }
-        }
-    }
+    const int32_t blk = a.bt[(int64_t)x.b * a.MB + key0 / a.bs];
+    row = a.NB * a.bs;                     // past the pool: TMA fills zeros
+    if ((unsigned)blk < (unsigned)a.NB)
+        row = blk * a.bs + key0 % a.bs;
+    else
+        bad = true;
     return true;
 }
 
-// One tile (K or V) into a stage: one box per 64-column block, or with kBoxed
-// and a cached tile one box per block of the pool, stacked.
-template <int D, bool kBoxed>
+// One tile (K or V) into a stage: one box per 64-column block.
+template <int D>
 __device__ __forceinline__ void load_tile(unsigned char* dst, const CUtensorMap* map,
-                                          uint64_t* bar, int kvh, bool cached, int32_t row,
-                                          const int32_t* rows, int32_t bs) {
-    constexpr int kBlocks = D / 64;
-    if (!(kBoxed && cached)) {
-        for (int hf = 0; hf < kBlocks; ++hf)
-            tma_load_3d(dst + hf * kHalf, map, bar, hf * 64, kvh, row);
-    } else {
-#pragma unroll
-        for (int u = 0; u < kMaxBoxes; ++u)
-            if (u * bs < kBN)
-#pragma unroll
-                for (int hf = 0; hf < kBlocks; ++hf)
-                    tma_load_3d(dst + hf * kHalf + u * bs * 128, map, bar, hf * 64, kvh, rows[u]);
-    }
+                                          uint64_t* bar, int kvh, int32_t row) {
+    for (int hf = 0; hf < D / 64; ++hf)
+        tma_load_3d(dst + hf * kHalf, map, bar, hf * 64, kvh, row);
 }
 
 // 16 bytes global -> shared with cp.async; `bytes` 0 writes zeros and reads
@@ -286,50 +249,57 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
-// Gathers cached tile j of item x (keys 128j .. 128j+127 of the prefix) into
-// a K and a V stage: lane l copies rows l, l+32, l+64, l+96, each 16-byte
-// chunk c of a row to where a 128-byte-swizzled TMA box would put it (64-column
-// block c/8, row r, chunk (c%8) ^ (r%8)).  Keys past the prefix or in a block
-// outside the pool read zeros; the latter set `bad`.
+// Gathers cached tile j of item x (keys 128j .. 128j+127 of the prefix) of
+// one pool (K or V) into a stage, each 16-byte chunk c of row r where a
+// 128-byte-swizzled TMA box would put it (64-column block c/8, row r, chunk
+// (c%8) ^ (r%8)).  Lane l resolves rows l, l+32, l+64, l+96 through the block
+// table; then each warp instruction copies whole rows (D/8 consecutive lanes
+// per row).  Keys past the prefix or in a block outside the pool read zeros;
+// the latter set `bad`.
 template <int D>
-__device__ __forceinline__ void gather_cached_tile(const PrefillArgs& a, const Item& x, int32_t j,
-                                                   int32_t kvh, unsigned char* kdst,
-                                                   unsigned char* vdst, int lane, bool& bad) {
+__device__ __forceinline__ void gather_cached_rows(const PrefillArgs& a, const Item& x, int32_t j,
+                                                   int32_t kvh, const __nv_bfloat16* pool,
+                                                   unsigned char* dst, int lane, bool& bad) {
+    constexpr int kChunks = D / 8;              // 16-byte chunks of a row
+    constexpr int kRowsPer = 32 / kChunks;      // rows one warp instruction covers
+    int64_t src[kBN / 32];                      // element offset of the row, or -1
 #pragma unroll
-    for (int rr = 0; rr < kBN / 32; ++rr) {
-        const int r = lane + 32 * rr;
-        const int32_t key = j * kBN + r;
-        int32_t blk = -1;
+    for (int g = 0; g < kBN / 32; ++g) {
+        const int32_t key = j * kBN + g * 32 + lane;
+        src[g] = -1;
         if (key < x.c) {
-            blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
-            if ((unsigned)blk >= (unsigned)a.NB) {
+            const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
+            if ((unsigned)blk < (unsigned)a.NB)
+                src[g] = (((int64_t)blk * a.bs + key % a.bs) * a.Hkv + kvh) * D;
+            else
                 bad = true;
-                blk = -1;
-            }
         }
-        const uint32_t bytes = blk >= 0 ? 16u : 0u;
-        const int64_t src_row = blk >= 0 ? (int64_t)blk * a.bs + key % a.bs : 0;
-        const __nv_bfloat16* ksrc = a.kc + (src_row * a.Hkv + kvh) * D;
-        const __nv_bfloat16* vsrc = a.vc + (src_row * a.Hkv + kvh) * D;
+    }
+    const int c = lane % kChunks, sub = lane / kChunks;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
+    for (int g = 0; g < kBN / 32; ++g) {
+#pragma unroll 4
+        for (int i = 0; i < 32 / kRowsPer; ++i) {
+            const int rl = i * kRowsPer + sub;
+            const int64_t e = __shfl_sync(0xffffffffu, src[g], rl);
+            const int r = g * 32 + rl;
+            const uint32_t bytes = e >= 0 ? 16u : 0u;
+            const int64_t eo = (e >= 0 ? e : 0) + c * 8;
             const int off = (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-            cp_async16_zfill(kdst + off, ksrc + c * 8, bytes);
-            cp_async16_zfill(vdst + off, vsrc + c * 8, bytes);
+            cp_async16_zfill(dst + off, pool + eo, bytes);
         }
     }
 }
 
-// kLoad: how cached tiles are loaded (see kLoadTile); the two per-block
-// modes are instantiations of their own so the common one-box producer loop
-// carries none of their code.  kPolls: the waits take their
+// kLoad: how cached tiles are loaded (see kLoadTile); the gather is an
+// instantiation of its own so the one-box producer loops carry none of its
+// code.  kPolls: the waits take their
 // poll limit from the arguments (pkv_set_wait_poll_limit) instead of the
 // compile-time default, in instantiations of their own (a run-time limit in
 // the tight waits of the issuers cost the default kernel about 5%).
 template <int D, int kLoad, bool kPolls>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
-    constexpr bool kBoxed = kLoad == kLoadBoxes;
     constexpr bool kGather = kLoad == kLoadGather;
     const uint32_t polls = kPolls ? a.wait_polls : (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     constexpr int kTile = TcSmem<D>::kTile;
@@ -355,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         mbar_init(&s.o_free, 128);
         for (int q = 0; q < kItemRing; ++q) {
             mbar_init(&s.item_full[q], 1);
-            mbar_init(&s.item_empty[q], item_readers_for<kLoad>());
+            mbar_init(&s.item_empty[q], kItemReaders);
         }
         mbar_init(&s.mma_done, 2);
         mbar_init_fence();
@@ -371,18 +341,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     // if any role gave up: tiles into the ring, and Q tiles
     uint32_t tiles_issued = 0, q_issued = 0;
 
-    if (kGather && warp == 4) {
-        // ------------------------------------------------------ gather producer
-        // The whole warp: lane 0 claims items, loads Q and the chunk's own K/V
-        // tiles by TMA; every lane gathers cached tiles with cp.async, one
-        // commit group per tile.  A gathered tile's K and V barriers are
-        // arrived once its group has landed (wait_group, then a proxy fence so
-        // the tensor core sees the writes, then lane 0 arrives), one tile
-        // behind the copies being issued so two tiles are in flight.
+    if (kGather && (warp == 4 || warp == 7)) {
+        // ------------------------------------------------------ gather producers
+        // Warp 4 takes K (and claims the items and loads Q), warp 7 takes V.
+        // Each loads its tensor's tiles of the chunk's own rows by TMA (lane
+        // 0) and gathers cached tiles with cp.async (every lane), one commit
+        // group per tile.  A gathered tile's barrier is arrived once its group
+        // has landed (wait_group, then a proxy fence so the tensor core sees
+        // the writes, then lane 0 arrives), one tile behind the copies being
+        // issued so two tiles are in flight.
+        const bool k_side = warp == 4;
+        uint64_t* full = k_side ? s.k_full : s.v_full;
+        uint64_t* empty = k_side ? s.k_empty : s.v_empty;
+        const CUtensorMap* own = k_side ? &maps.k : &maps.v;
+        const __nv_bfloat16* pool = k_side ? a.kc : a.vc;
         if (lane == 0) {
-            tma_prefetch_desc(&maps.q);
-            tma_prefetch_desc(&maps.k);
-            tma_prefetch_desc(&maps.v);
+            if (k_side) tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(own);
         }
         uint32_t& T = tiles_issued;               // tiles whose barriers will complete
         uint32_t I = 0;
@@ -391,45 +366,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         auto land = [&](int st_) {
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&s.k_full[st_]);
-                mbar_arrive(&s.v_full[st_]);
-            }
+            if (lane == 0) mbar_arrive(&full[st_]);
         };
         for (; ok; ++I) {
-            const int qs = I % kItemRing;
-            if (I >= kItemRing && !(ok = warp_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1,
-                                                   &s.abort_flag, polls)))
-                break;
             int32_t it = 0;
-            if (lane == 0) {
-                it = atomicAdd(&a.sched[1], 1);
-                s.item_ring[qs] = it < n_items ? it : -1;
-                mbar_arrive(&s.item_full[qs]);
+            if (k_side) {
+                const int qs = I % kItemRing;
+                if (I >= kItemRing &&
+                    !(ok = warp_wait(&s.item_empty[qs], (I / kItemRing - 1) & 1,
+                                     &s.abort_flag, polls)))
+                    break;
+                if (lane == 0) {
+                    it = atomicAdd(&a.sched[1], 1);
+                    s.item_ring[qs] = it < n_items ? it : -1;
+                    mbar_arrive(&s.item_full[qs]);
+                }
+                it = __shfl_sync(0xffffffffu, it, 0);
+                if (it >= n_items) break;
+            } else {
+                if (!(ok = next_item(s, I, it, polls, true))) break;
+                if (it < 0) break;
             }
-            it = __shfl_sync(0xffffffffu, it, 0);
-            if (it >= n_items) break;
             const Item x = item_at(a, it);
             const int32_t kvh = x.h / a.G;
-            if (I > 0 && !(ok = warp_wait(&s.q_free, (I - 1) & 1, &s.abort_flag, polls))) break;
-            if (lane == 0) {
-                mbar_expect_tx(&s.q_full, kTile);
-                for (int hf = 0; hf < kBlocks; ++hf)
-                    tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
-                                x.q0 + x.m * kBM);
+            if (k_side) {
+                if (I > 0 && !(ok = warp_wait(&s.q_free, (I - 1) & 1, &s.abort_flag, polls)))
+                    break;
+                if (lane == 0) {
+                    mbar_expect_tx(&s.q_full, kTile);
+                    for (int hf = 0; hf < kBlocks; ++hf)
+                        tma_load_3d(s.q + hf * kHalf, &maps.q, &s.q_full, hf * 64, x.h,
+                                    x.q0 + x.m * kBM);
+                }
+                ++q_issued;
             }
-            ++q_issued;
             for (int32_t j = 0; j < x.n_tiles; ++j, ++T) {
                 const int st = T % kStages;
                 const uint32_t use = T / kStages;
-                if (use > 0 && !(ok = warp_wait(&s.k_empty[st], (use - 1) & 1, &s.abort_flag,
-                                                polls)))
+                if (use > 0 && !(ok = warp_wait(&empty[st], (use - 1) & 1, &s.abort_flag, polls)))
                     break;
-                if (use > 0 && !(ok = warp_wait(&s.v_empty[st], (use - 1) & 1, &s.abort_flag,
-                                                polls)))
-                    break;
+                unsigned char* dst = k_side ? s.k[st] : s.v[st];
                 if (j < x.n_cached) {
-                    gather_cached_tile<D>(a, x, j, kvh, s.k[st], s.v[st], lane, bad_block);
+                    gather_cached_rows<D>(a, x, j, kvh, pool, dst, lane, bad_block);
                     cp_async_commit();
                     if (pend >= 0) {
                         cp_async_wait<1>();          // the tile before this one has landed
@@ -445,14 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     }
                     if (lane == 0) {
                         const int32_t row = x.q0 + (j - x.n_cached) * kBN;
-                        mbar_expect_tx(&s.k_full[st], kTile);
+                        mbar_expect_tx(&full[st], kTile);
                         for (int hf = 0; hf < kBlocks; ++hf)
-                            tma_load_3d(s.k[st] + hf * kHalf, &maps.k, &s.k_full[st], hf * 64,
-                                        kvh, row);
-                        mbar_expect_tx(&s.v_full[st], kTile);
-                        for (int hf = 0; hf < kBlocks; ++hf)
-                            tma_load_3d(s.v[st] + hf * kHalf, &maps.v, &s.v_full[st], hf * 64,
-                                        kvh, row);
+                            tma_load_3d(dst + hf * kHalf, own, &full[st], hf * 64, kvh, row);
                     }
                 }
             }
@@ -506,28 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     if (use > 0 && !(ok = mbar_wait(&s.k_empty[st], (use - 1) & 1,
                             &s.abort_flag, polls)))
                         break;
-                    int32_t row, rows[kMaxBoxes];
-                    const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
+                    int32_t row;
+                    const bool cached = tile_source(a, x, j, row, bad_block);
                     mbar_expect_tx(&s.k_full[st], kTile);
-                    load_tile<D, kBoxed>(s.k[st], cached ? &maps.kc : &maps.k, &s.k_full[st], kvh,
-                                         cached, row, rows, a.bs);
-                    if constexpr (kLoad != kLoadTile) {
-                        if (use > 0 &&
-                            !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
-                                    &s.abort_flag, polls))) {
-                            mbar_drain(&s.k_full[st], use & 1);   // this tile's K is in flight
-                            break;
-                        }
-                        mbar_expect_tx(&s.v_full[st], kTile);
-                        load_tile<D, kBoxed>(s.v[st], cached ? &maps.vc : &maps.v, &s.v_full[st],
-                                             kvh, cached, row, rows, a.bs);
-                    }
+                    load_tile<D>(s.k[st], cached ? &maps.kc : &maps.k, &s.k_full[st], kvh, row);
                 }
             }
             if (bad_block) pkv::report(a.status, PKV_STATUS_BAD_BLOCK_ID);
             if (!ok) give_up(s, a.status);
         }
-    } else if (kLoad == kLoadTile && warp == 7) {
+    } else if (warp == 7) {
         // ------------------------------------------------------------ V producer
         // V tiles on their own thread: a V stage waits for its P V, and in
         // the producer's loop that wait held back the next K tile
@@ -547,11 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                     if (use > 0 && !(ok = mbar_wait(&s.v_empty[st], (use - 1) & 1,
                             &s.abort_flag, polls)))
                         break;
-                    int32_t row, rows[kMaxBoxes];
-                    const bool cached = tile_source<kBoxed>(a, x, j, row, rows, bad_block);
+                    int32_t row;
+                    const bool cached = tile_source(a, x, j, row, bad_block);
                     mbar_expect_tx(&s.v_full[st], kTile);
-                    load_tile<D, kBoxed>(s.v[st], cached ? &maps.vc : &maps.v, &s.v_full[st], kvh,
-                                         cached, row, rows, a.bs);
+                    load_tile<D>(s.v[st], cached ? &maps.vc : &maps.v, &s.v_full[st], kvh, row);
                 }
             }
             if (!ok) give_up(s, a.status);
@@ -818,15 +778,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (s.abort_flag && lane == 0 && (warp == 4 || (kLoad == kLoadTile && warp == 7))) {
+    if (s.abort_flag && lane == 0 && (warp == 4 || warp == 7)) {
         // some role gave up: every copy this producer issued lands before the
         // CTA exits (a consumer may have given up after the last one was issued)
         const bool k_side = warp == 4;
         for (uint32_t back = 1; back <= (uint32_t)kStages && back <= tiles_issued; ++back) {
             const uint32_t t = tiles_issued - back;
-            if (k_side) mbar_drain(&s.k_full[t % kStages], (t / kStages) & 1);
-            if (!k_side || kLoad != kLoadTile)
-                mbar_drain(&s.v_full[t % kStages], (t / kStages) & 1);
+            mbar_drain(k_side ? &s.k_full[t % kStages] : &s.v_full[t % kStages],
+                       (t / kStages) & 1);
         }
         if (k_side && q_issued > 0) mbar_drain(&s.q_full, (q_issued - 1) & 1);
     }
@@ -834,31 +793,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 }
 
 // ---------------------------------------------------------------- host side
-// [rows, heads, D] bf16, box 64 x 1 head x box_rows rows.
-bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int head_dim,
-                 int box_rows = kBN) {
-    return pkv::tma_encode_rows(m, base, rows, heads, head_dim, box_rows);
+// [rows, heads, D] bf16, box 64 x 1 head x 128 rows.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int head_dim) {
+    return pkv::tma_encode_rows(m, base, rows, heads, head_dim, kBN);
 }
 
 // The load mode of a call's cached tiles (see kLoadTile).
 int load_mode(const PrefillArgs& a) {
-    if (a.bt == nullptr || a.bs % kBN == 0) return kLoadTile;
-    if (a.bs % 8 == 0 && kBN % a.bs == 0) return kLoadBoxes;
-    return kLoadGather;
+    return a.bt == nullptr || a.bs % kBN == 0 ? kLoadTile : kLoadGather;
 }
 
 template <int D>
 int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillPrologue* pre) {
     using Kernel = void (*)(const TcMaps, const PrefillArgs);
-    static const Kernel kernels[3][2] = {
+    static const Kernel kernels[2][2] = {
         {prefill_tc_kernel<D, kLoadTile, false>, prefill_tc_kernel<D, kLoadTile, true>},
-        {prefill_tc_kernel<D, kLoadBoxes, false>, prefill_tc_kernel<D, kLoadBoxes, true>},
         {prefill_tc_kernel<D, kLoadGather, false>, prefill_tc_kernel<D, kLoadGather, true>}};
     const int smem = (int)sizeof(TcSmem<D>) + 1024;
     const int mode = load_mode(a);
     const int custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS ? 1 : 0;
     const Kernel kernel = kernels[mode][custom];
-    static std::atomic<uint64_t> configured[6];
+    static std::atomic<uint64_t> configured[4];
     if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[mode * 2 + custom]))
         return PKV_ERR_CUDA;
     a.tile_m = kBM;
@@ -874,8 +829,7 @@ int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(mode == kLoadTile ? threads_for<kLoadTile>() : threads_for<kLoadBoxes>(),
-                        1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -900,10 +854,9 @@ int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
         !encode_rows(&maps.k, a.k, a.total_q, a.Hkv, head_dim) ||
         !encode_rows(&maps.v, a.v, a.total_q, a.Hkv, head_dim))
         return PKV_ERR_CUDA;
-    if (a.bt && load_mode(a) != kLoadGather) {
-        const int box = a.bs % kBN == 0 ? kBN : a.bs;
-        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, box) ||
-            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, box))
+    if (a.bt && load_mode(a) == kLoadTile) {
+        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim) ||
+            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim))
             return PKV_ERR_CUDA;
     } else {
         maps.kc = maps.k;

@@ -3,9 +3,9 @@
 
 pkv_kv_store_paged_prefill_varlen must leave the cache exactly as pkv_kv_store
 leaves it and give exactly the output of pkv_paged_prefill_varlen (same
-kernels, chained launches), with each way the tcgen05 kernel loads cached
-tiles (one TMA box per tile for block sizes that are multiples of 128, one box
-per block for 8..64, rows gathered with cp.async for 4 and 48), eagerly and
+kernels, chained launches), with both ways the tcgen05 kernel loads cached
+tiles (TMA boxes for block sizes that are multiples of 128, rows gathered with
+cp.async for the others: 16, 32, 4, 48 here), eagerly and
 replayed from a CUDA graph; its output also matches the float64 oracle."""
 import numpy as np
 import pytest

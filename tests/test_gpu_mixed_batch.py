@@ -22,9 +22,9 @@ from test_gpu_prefill import make_case
 
 pytestmark = pytest.mark.gpu
 
-# (Hq, Hkv, D, block size): TMA decode + tcgen05 prefill; register decode +
-# tcgen05 prefill with a box per block; head_dim 64 on both TMA paths;
-# register decode + tcgen05 prefill with gathered cached rows
+# (Hq, Hkv, D, block size): TMA decode + tcgen05 prefill reading cached tiles
+# as TMA boxes; register decode + tcgen05 prefill gathering cached rows with
+# cp.async (16, 48); head_dim 64 with TMA decode and gathered prefill rows
 SHAPES = [(8, 2, 128, 256), (8, 2, 128, 16), (4, 1, 64, 64), (6, 3, 128, 48)]
 
 

@@ -72,9 +72,9 @@ def test_tiny_with_and_without_block_tables(cuda):
     assert torch.equal(outs[0], outs[1])
 
 
-# the tcgen05 kernel's three ways of loading a cached 128-key tile: one TMA box
-# (block sizes that are multiples of 128), one box per block (8, 16, 32, 64), or
-# rows gathered by the producer warp with cp.async (4, 48)
+# the tcgen05 kernel's two ways of loading a cached 128-key tile: one TMA box
+# per 64-column block (block sizes that are multiples of 128), or rows gathered
+# by the producer warps with cp.async (any other: 4, 8, 16, 32, 48, 64)
 @pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 16), (4, 1, 64, 4), (6, 3, 128, 256),
                                          (2, 2, 64, 256), (16, 4, 128, 128), (8, 2, 128, 8),
                                          (4, 4, 128, 32), (8, 1, 128, 64), (4, 2, 128, 48),

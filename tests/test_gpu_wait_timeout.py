@@ -55,8 +55,8 @@ def test_decode_gives_up_then_recovers(cuda, wait_limit):
     U.assert_close(U.f64(out), ref, "decode after the timeouts")
 
 
-# block size 256: one TMA box per cached tile; 64: a cached tile from two
-# boxes; 48: its rows gathered by the producer warp with cp.async
+# block size 256: cached tiles as TMA boxes; 64 and 48: their rows gathered
+# by the producer warps with cp.async
 @pytest.mark.parametrize("bs,cached", [(256, [256, 0, 512]), (64, [128, 64, 0]),
                                        (48, [96, 5, 0])])
 def test_prefill_gives_up_then_recovers(cuda, wait_limit, bs, cached):

@@ -170,6 +170,27 @@ def time_graph(g, iters, torch):
     return s.elapsed_time(e) / iters * 1e-3          # seconds per replay
 
 
+def time_graphs_paired(ga, gb, pairs, torch):
+    """Mean seconds per replay of two graphs timed in alternation (a, b, a,
+    b, ...), CUDA events around each replay, so drift of clock or
+    temperature over the run falls on both alike; also the median of the
+    per-pair differences b - a."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(2 * pairs)]
+    torch.cuda.synchronize()
+    for i in range(pairs):
+        for j, g in enumerate((ga, gb)):
+            s, e = ev[2 * i + j]
+            s.record()
+            g.replay()
+            e.record()
+    torch.cuda.synchronize()
+    ta = [ev[2 * i][0].elapsed_time(ev[2 * i][1]) * 1e-3 for i in range(pairs)]
+    tb = [ev[2 * i + 1][0].elapsed_time(ev[2 * i + 1][1]) * 1e-3 for i in range(pairs)]
+    diff = sorted(b - a for a, b in zip(ta, tb))
+    return sum(ta) / pairs, sum(tb) / pairs, diff[pairs // 2]
+
+
 def hbm_read_reference(torch, dev, nbytes=2 << 30, reps=10):
     """A read-only stream for context beside the copy peak: the best of
     `reps` torch reductions (sum and max) over a 2 GiB fp32 tensor, in GB/s
@@ -688,9 +709,10 @@ def bench_step(pkv, W, torch, dev, pk):
     for gg in (gs, gd, gm, gf, gz, gpx):
         for _ in range(3):
             gg.replay()
-    t_s, t_d, t_m, t_f = (time_graph(gs, 200, torch), time_graph(gd, 30, torch),
-                          time_graph(gm, 50, torch), time_graph(gf, 30, torch))
-    t_z = time_graph(gz, 30, torch)
+    t_s, t_m, t_f = (time_graph(gs, 200, torch), time_graph(gm, 50, torch),
+                     time_graph(gf, 30, torch))
+    # the decode alone and the store + decode call, replay by replay in turn
+    t_d, t_z, dz_med = time_graphs_paired(gd, gz, 40, torch)
     t_px = time_graph(gpx, 50, torch)
     b_s = 4.0 * w.k_new.numel() * 2
     b_d = decode_bytes(w.context_lens.tolist(), spec.num_q_heads, spec.num_kv_heads,
@@ -702,13 +724,16 @@ def bench_step(pkv, W, torch, dev, pk):
         "decode_us": round(t_d * 1e6, 2), "decode_gbs": round(b_d / t_d / 1e9, 1),
         "decode_frac_hbm": round(b_d / t_d / 1e9 / pk["hbm"], 4),
         "fused_store_decode_us": round(t_z * 1e6, 2),
+        "fused_minus_decode_median_us": round(dz_med * 1e6, 2),
         "sample_us": round(t_m * 1e6, 2), "sample_gbs": round(b_m / t_m / 1e9, 1),
         "sample_frac_hbm": round(b_m / t_m / 1e9 / pk["hbm"], 4),
         "sample_philox_us": round(t_px * 1e6, 2),
         "sample_philox_gbs": round((b_m / 2) / t_px / 1e9, 1),
         "sample_philox_note": "noise drawn in the kernel (Philox4x32-10): logits and "
                               "temperatures only, 4 bytes per entry",
-        "timing": "CUDA graph replays, CUDA events; kv_store re-writes the same slots"}
+        "timing": "CUDA graph replays, CUDA events; kv_store re-writes the same slots; "
+                  "decode_us and fused_store_decode_us: 40 replays of each in alternation, "
+                  "events around each replay (mean; the difference as the median over pairs)"}
     return res
 
 

@@ -21,6 +21,7 @@ replica; value = bytes of all ranks / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -1057,8 +1058,11 @@ def profile_case(name: str, calls: int):
         for _ in range(calls):
             pkv.paged_decode(w.q, w.k_cache, w.v_cache, bt, ctx, w.scale, w.max_context_len,
                              out=out, workspace=ws)
-    elif name == "prefill-8b":
+    elif name in ("prefill-8b", "prefill-8b-bs16"):
         spec = W.PREFILL_8B
+        if name == "prefill-8b-bs16":
+            # the same prompts on 16-slot cache blocks: cached rows are gathered
+            spec = dataclasses.replace(spec, block_size=16, max_cached_blocks=64)
         w = W.prefill_workload(spec)
         st = w.steps[0]
         kc, vc = w.k_cache0.to(dev), w.v_cache0.to(dev)
@@ -1111,7 +1115,7 @@ def main():
                     help="seconds of wall time per multi-core CPU oracle leg")
     ap.add_argument("--profile", default=None,
                     help="run a small case for ncu instead of the benchmark: decode-0.6b, "
-                         "prefill-8b, sample or mixed-8b (calls = --steps)")
+                         "prefill-8b, prefill-8b-bs16, sample or mixed-8b (calls = --steps)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

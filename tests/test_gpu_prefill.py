@@ -1,4 +1,5 @@
 """paged_prefill_varlen on the GPU against the float64 oracle."""
+import dataclasses
 import math
 
 import numpy as np
@@ -143,9 +144,15 @@ def test_chunked_walkthrough_equals_oneshot_on_gpu(cuda):
     U.assert_close(U.f64(chunked), ref, "chunked")
 
 
-def test_prefill_8b_steps_sampled_rows(cuda):
+# block size 256: cached tiles as TMA boxes; 16: the same prompts (prefixes of
+# up to 1024 keys) with every cached tile's rows gathered by cp.async
+@pytest.mark.parametrize("bs", [256, 16])
+def test_prefill_8b_steps_sampled_rows(cuda, bs):
     pkv = U.lib()
-    w = W.prefill_workload(W.PREFILL_8B)
+    spec = W.PREFILL_8B
+    if bs != spec.block_size:
+        spec = dataclasses.replace(spec, block_size=bs, max_cached_blocks=1024 // bs)
+    w = W.prefill_workload(spec)
     kc, vc = w.k_cache0.to(cuda), w.v_cache0.to(cuda)
     okc, ovc = U.bits(w.k_cache0), U.bits(w.v_cache0)
     rng = np.random.default_rng(0)

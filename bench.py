@@ -1047,8 +1047,11 @@ def profile_case(name: str, calls: int):
     pkv.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if name == "decode-0.6b":
+    if name in ("decode-0.6b", "decode-0.6b-bs16"):
         spec = W.DECODE_0P6B
+        if name == "decode-0.6b-bs16":
+            # the same batch on 16-slot cache blocks: the register-load split kernel
+            spec = dataclasses.replace(spec, block_size=16)
         w = W.decode_workload(spec, device=dev)
         bt, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
         out = torch.empty_like(w.q)
@@ -1115,7 +1118,8 @@ def main():
                     help="seconds of wall time per multi-core CPU oracle leg")
     ap.add_argument("--profile", default=None,
                     help="run a small case for ncu instead of the benchmark: decode-0.6b, "
-                         "prefill-8b, prefill-8b-bs16, sample or mixed-8b (calls = --steps)")
+                         "decode-0.6b-bs16, prefill-8b, prefill-8b-bs16, sample or mixed-8b "
+                         "(calls = --steps)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

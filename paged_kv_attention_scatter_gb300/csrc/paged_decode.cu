@@ -194,6 +194,24 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
         float m_run = -INFINITY, l_run = 0.f;
         bool bad_block = false;
 
+        // Block sizes that are multiples of 16: one block-table entry covers a
+        // warp step.  Others: lane l resolves key step + (l & 15) to its row
+        // offset (-1 past the chunk or for a bad block id), one lookup and one
+        // division per lane, and each fragment row is shuffled from the lane
+        // that holds it (six lookups per lane were 20% slower at block size 8).
+        auto lookup_row = [&](int32_t st) {
+            const int32_t key = st + (lane & 15);
+            int64_t row = -1;
+            if (key < key_end) {
+                const int32_t blk = bt_row[key / a.bs];
+                if ((unsigned)blk < (unsigned)a.NB)
+                    row = ((int64_t)blk * a.bs + key % a.bs) * row_elems;
+                else
+                    bad_block = true;
+            }
+            return row;
+        };
+
         for (int32_t step = key0 + warp * kStep; step < key_end; step += kWarps * kStep) {
             // ---- row addresses (nullptr: not loaded, treated as masked) ----
             const __nv_bfloat16* krow[2];
@@ -218,28 +236,16 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
                                   ? vbase + r0 + (int64_t)(vkey[r] - step) * row_elems
                                   : nullptr;
             } else {
+                const int64_t row = lookup_row(step);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int key = step + r * 8 + g;
-                    krow[r] = nullptr;
-                    if (key < key_end) {
-                        const int32_t blk = bt_row[key / a.bs];
-                        if ((unsigned)blk < (unsigned)a.NB)
-                            krow[r] = kbase + ((int64_t)blk * a.bs + key % a.bs) * row_elems;
-                        else
-                            bad_block = true;
-                    }
+                    const int64_t rr = __shfl_sync(0xffffffffu, row, r * 8 + g);
+                    krow[r] = rr >= 0 ? kbase + rr : nullptr;
                 }
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    vrow[r] = nullptr;
-                    if (vkey[r] < key_end) {
-                        const int32_t blk = bt_row[vkey[r] / a.bs];
-                        if ((unsigned)blk < (unsigned)a.NB)
-                            vrow[r] = vbase + ((int64_t)blk * a.bs + vkey[r] % a.bs) * row_elems;
-                        else
-                            bad_block = true;
-                    }
+                    const int64_t rr = __shfl_sync(0xffffffffu, row, vkey[r] - step);
+                    vrow[r] = rr >= 0 ? vbase + rr : nullptr;
                 }
             }
             // ---- loads: K rows step+g, step+8+g; V rows 2t, 2t+1, 2t+8, 2t+9 ----

@@ -1,7 +1,7 @@
 // paged_prefill_varlen on the 5th-generation tensor cores: tcgen05.mma with
 // TMEM accumulators, Q/K/V tiles staged by TMA (cached tiles gathered row by
-// row with cp.async when the block size is not a multiple of 128), for
-// head_dim 128 or 64 and any block size.
+// row with cp.async, in part or whole, when the block size is not a multiple
+// of 128), for head_dim 128 or 64 and any block size.
 //
 // What it computes is stated in prefill.cu (causal varlen prefill over a
 // prefix-cached paged cache, uml.org.cn walk-through §2.4 / §3.2).
@@ -14,11 +14,14 @@
 //   * cached tiles u = 0 .. ceil(c/128)-1: keys 128u .. 128u+127 of the
 //     prefix, per half of head_dim one TMA box at row
 //     block_tables[b][128u / bs] * bs + (128u % bs) of the pool when bs is a
-//     multiple of 128; for any other block size the producer warps gather the
-//     tile's rows with 16-byte cp.async copies into the same swizzled layout
-//     (keys past the prefix read zeros either way).  Per-block TMA boxes
-//     (8..64 rows, stacked) measured slower than the gather at every such
-//     block size, and a box below 8 rows would start inside a swizzle atom;
+//     multiple of 128.  For block sizes 8, 16, 32 and 64 the K tile is one
+//     box per cache block (bs rows, stacked at row offsets that are multiples
+//     of 8, the swizzle atom) and the V producer warp gathers the V tile's
+//     rows with 16-byte cp.async copies into the same swizzled layout; for any
+//     other block size both producer warps gather (keys past the prefix read
+//     zeros in every mode).  Boxes for both tensors, or the gather for both,
+//     measured 3-6% slower than this split at 8..64, and a box below 8 rows
+//     would start inside a swizzle atom;
 //   * new tiles t = 0 .. m: the chunk's own k/v rows q0 + 128t ..; tile t == m
 //     is the diagonal (causal mask col <= row), tiles t > m are never visible.
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
@@ -41,7 +44,8 @@
 //   warp 7     TMA producer of the V tiles (one thread, three stages), a stage
 //              refilled once its P V is done; on its own warp so that wait
 //              never holds back a K tile.  When cached tiles are gathered,
-//              all 32 lanes of warps 4 and 7 take part (K and V respectively).
+//              all 32 lanes of warps 4 and 7 take part (K and V respectively;
+//              with per-block K boxes, warp 4's lanes look up the blocks).
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for
@@ -80,9 +84,11 @@ constexpr int kBN = pkv::kPrefillTileK;  // keys per tile
 constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
 constexpr int kThreads = 256;
 // How a cached 128-key tile reaches shared memory, by block size: one TMA box
-// per 64-column block (a multiple of 128), or rows gathered by the producer
-// warps with cp.async (any other block size).
-constexpr int kLoadTile = 0, kLoadGather = 1;
+// per 64-column block (a multiple of 128); K as one box per cache block and V
+// rows gathered with cp.async (8, 16, 32, 64: the copy unit and the load path
+// each carry one tensor); or both gathered by the producer warps with cp.async
+// (any other block size).
+constexpr int kLoadTile = 0, kLoadGather = 1, kLoadHybrid = 2;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
 constexpr int kItemReaders = 7;          // V producer, Q K^T and P V issuers, 4 softmax warps
@@ -300,7 +306,8 @@ __device__ __forceinline__ void gather_cached_rows(const PrefillArgs& a, const I
 template <int D, int kLoad, bool kPolls>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
-    constexpr bool kGather = kLoad == kLoadGather;
+    constexpr bool kGather = kLoad != kLoadTile;  // the producer warps' lanes gather
+    constexpr bool kBoxK = kLoad == kLoadHybrid;   // ... except K, as per-block boxes
     const uint32_t polls = kPolls ? a.wait_polls : (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     constexpr int kTile = TcSmem<D>::kTile;
     constexpr int kBlocks = D / 64;               // 64-column blocks of a tile
@@ -355,8 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         uint64_t* empty = k_side ? s.k_empty : s.v_empty;
         const CUtensorMap* own = k_side ? &maps.k : &maps.v;
         const __nv_bfloat16* pool = k_side ? a.kc : a.vc;
+        const bool boxes = kBoxK && k_side;     // cached K tiles as per-block boxes
         if (lane == 0) {
             if (k_side) tma_prefetch_desc(&maps.q);
+            if (boxes) tma_prefetch_desc(&maps.kc);
             tma_prefetch_desc(own);
         }
         uint32_t& T = tiles_issued;               // tiles whose barriers will complete
@@ -406,7 +415,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                 if (use > 0 && !(ok = warp_wait(&empty[st], (use - 1) & 1, &s.abort_flag, polls)))
                     break;
                 unsigned char* dst = k_side ? s.k[st] : s.v[st];
-                if (j < x.n_cached) {
+                if (boxes && j < x.n_cached) {
+                    // lane u resolves cache block u of the tile (128 / bs of
+                    // them, each a box of bs rows stacked at row u * bs, an
+                    // 8-row swizzle atom boundary); keys past the prefix, or a
+                    // block id outside the pool, read the zeros past the pool
+                    const int nbox = kBN / a.bs;
+                    int32_t my_row = a.NB * a.bs;
+                    if (lane < nbox) {
+                        const int32_t key = j * kBN + lane * a.bs;
+                        if (key < x.c) {
+                            const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
+                            if ((unsigned)blk < (unsigned)a.NB)
+                                my_row = blk * a.bs;
+                            else
+                                bad_block = true;
+                        }
+                    }
+                    if (lane == 0) mbar_expect_tx(&full[st], kTile);
+                    for (int u = 0; u < nbox; ++u) {
+                        const int32_t row = __shfl_sync(0xffffffffu, my_row, u);
+                        if (lane == 0)
+                            for (int hf = 0; hf < kBlocks; ++hf)
+                                tma_load_3d(dst + hf * kHalf + u * a.bs * 128, &maps.kc,
+                                            &full[st], hf * 64, kvh, row);
+                    }
+                } else if (j < x.n_cached) {
                     gather_cached_rows<D>(a, x, j, kvh, pool, dst, lane, bad_block);
                     cp_async_commit();
                     if (pend >= 0) {
@@ -793,27 +827,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 }
 
 // ---------------------------------------------------------------- host side
-// [rows, heads, D] bf16, box 64 x 1 head x 128 rows.
-bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int head_dim) {
-    return pkv::tma_encode_rows(m, base, rows, heads, head_dim, kBN);
+// [rows, heads, D] bf16, box 64 x 1 head x box_rows rows.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int head_dim,
+                 int box_rows = kBN) {
+    return pkv::tma_encode_rows(m, base, rows, heads, head_dim, box_rows);
 }
 
 // The load mode of a call's cached tiles (see kLoadTile).
 int load_mode(const PrefillArgs& a) {
-    return a.bt == nullptr || a.bs % kBN == 0 ? kLoadTile : kLoadGather;
+    if (a.bt == nullptr || a.bs % kBN == 0) return kLoadTile;
+    if (a.bs % 8 == 0 && kBN % a.bs == 0) return kLoadHybrid;
+    return kLoadGather;
 }
 
 template <int D>
 int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillPrologue* pre) {
     using Kernel = void (*)(const TcMaps, const PrefillArgs);
-    static const Kernel kernels[2][2] = {
+    static const Kernel kernels[3][2] = {
         {prefill_tc_kernel<D, kLoadTile, false>, prefill_tc_kernel<D, kLoadTile, true>},
-        {prefill_tc_kernel<D, kLoadGather, false>, prefill_tc_kernel<D, kLoadGather, true>}};
+        {prefill_tc_kernel<D, kLoadGather, false>, prefill_tc_kernel<D, kLoadGather, true>},
+        {prefill_tc_kernel<D, kLoadHybrid, false>, prefill_tc_kernel<D, kLoadHybrid, true>}};
     const int smem = (int)sizeof(TcSmem<D>) + 1024;
     const int mode = load_mode(a);
     const int custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS ? 1 : 0;
     const Kernel kernel = kernels[mode][custom];
-    static std::atomic<uint64_t> configured[4];
+    static std::atomic<uint64_t> configured[6];
     if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[mode * 2 + custom]))
         return PKV_ERR_CUDA;
     a.tile_m = kBM;
@@ -854,10 +892,16 @@ int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
         !encode_rows(&maps.k, a.k, a.total_q, a.Hkv, head_dim) ||
         !encode_rows(&maps.v, a.v, a.total_q, a.Hkv, head_dim))
         return PKV_ERR_CUDA;
-    if (a.bt && load_mode(a) == kLoadTile) {
+    const int mode = a.bt ? load_mode(a) : kLoadTile;
+    if (a.bt && mode == kLoadTile) {
         if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim) ||
             !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim))
             return PKV_ERR_CUDA;
+    } else if (mode == kLoadHybrid) {
+        // K boxes of one cache block; V is gathered
+        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, a.bs))
+            return PKV_ERR_CUDA;
+        maps.vc = maps.v;
     } else {
         maps.kc = maps.k;
         maps.vc = maps.v;

@@ -16,12 +16,14 @@
 //     block_tables[b][128u / bs] * bs + (128u % bs) of the pool when bs is a
 //     multiple of 128.  For block sizes 8, 16, 32 and 64 the K tile is one
 //     box per cache block (bs rows, stacked at row offsets that are multiples
-//     of 8, the swizzle atom) and the V producer warp gathers the V tile's
-//     rows with 16-byte cp.async copies into the same swizzled layout; for any
-//     other block size both producer warps gather (keys past the prefix read
-//     zeros in every mode).  Boxes for both tensors, or the gather for both,
-//     measured 3-6% slower than this split at 8..64, and a box below 8 rows
-//     would start inside a swizzle atom;
+//     of 8, the swizzle atom), and so are the first 96 (bs 16, 32) or 64
+//     (bs 8, 64) rows of the V tile, whose other rows the V producer warp
+//     gathers with 16-byte cp.async copies into the same swizzled layout: the
+//     copy unit and the load path share the bytes.  For any other block size
+//     both producer warps gather (keys past the prefix read zeros in every
+//     mode).  Boxes for everything, or the gather for everything, measured
+//     15-30% slower at 16..64, and a box below 8 rows would start inside a
+//     swizzle atom;
 //   * new tiles t = 0 .. m: the chunk's own k/v rows q0 + 128t ..; tile t == m
 //     is the diagonal (causal mask col <= row), tiles t > m are never visible.
 // Masked keys get -inf scores; V rows of masked cached keys are zeroed in
@@ -45,7 +47,9 @@
 //              refilled once its P V is done; on its own warp so that wait
 //              never holds back a K tile.  When cached tiles are gathered,
 //              all 32 lanes of warps 4 and 7 take part (K and V respectively;
-//              with per-block K boxes, warp 4's lanes look up the blocks).
+//              with per-block boxes, their lanes look up the blocks and lane
+//              0 issues the boxes; a V stage's barrier then expects the boxes'
+//              bytes and is arrived once the gathered rows have landed).
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for
@@ -84,11 +88,12 @@ constexpr int kBN = pkv::kPrefillTileK;  // keys per tile
 constexpr int kHalf = kBM * 128;         // one 64-column block of a tile
 constexpr int kThreads = 256;
 // How a cached 128-key tile reaches shared memory, by block size: one TMA box
-// per 64-column block (a multiple of 128); K as one box per cache block and V
-// rows gathered with cp.async (8, 16, 32, 64: the copy unit and the load path
-// each carry one tensor); or both gathered by the producer warps with cp.async
-// (any other block size).
-constexpr int kLoadTile = 0, kLoadGather = 1, kLoadHybrid = 2;
+// per 64-column block (a multiple of 128); K as one box per cache block and
+// the first 64 (block sizes 8, 64) or 96 (16, 32) rows of V the same way, the
+// rest of V gathered with cp.async, so the copy unit and the load path share
+// the bytes; or both tensors gathered by the producer warps (any other block
+// size).
+constexpr int kLoadTile = 0, kLoadGather = 1, kLoadSplit64 = 2, kLoadSplit96 = 3;
 constexpr int kStages = 3;               // K/V ring depth
 constexpr int kItemRing = 4;             // work items handed from the producer to the others
 constexpr int kItemReaders = 7;          // V producer, Q K^T and P V issuers, 4 softmax warps
@@ -261,8 +266,8 @@ __device__ __forceinline__ void cp_async_wait() {
 // (c%8) ^ (r%8)).  Lane l resolves rows l, l+32, l+64, l+96 through the block
 // table; then each warp instruction copies whole rows (D/8 consecutive lanes
 // per row).  Keys past the prefix or in a block outside the pool read zeros;
-// the latter set `bad`.
-template <int D>
+// the latter set `bad`.  kG0 > 0 gathers only rows 32 kG0 .. 127.
+template <int D, int kG0 = 0>
 __device__ __forceinline__ void gather_cached_rows(const PrefillArgs& a, const Item& x, int32_t j,
                                                    int32_t kvh, const __nv_bfloat16* pool,
                                                    unsigned char* dst, int lane, bool& bad) {
@@ -270,7 +275,7 @@ __device__ __forceinline__ void gather_cached_rows(const PrefillArgs& a, const I
     constexpr int kRowsPer = 32 / kChunks;      // rows one warp instruction covers
     int64_t src[kBN / 32];                      // element offset of the row, or -1
 #pragma unroll
-    for (int g = 0; g < kBN / 32; ++g) {
+    for (int g = kG0; g < kBN / 32; ++g) {
         const int32_t key = j * kBN + g * 32 + lane;
         src[g] = -1;
         if (key < x.c) {
@@ -283,7 +288,7 @@ __device__ __forceinline__ void gather_cached_rows(const PrefillArgs& a, const I
     }
     const int c = lane % kChunks, sub = lane / kChunks;
 #pragma unroll
-    for (int g = 0; g < kBN / 32; ++g) {
+    for (int g = kG0; g < kBN / 32; ++g) {
 #pragma unroll 4
         for (int i = 0; i < 32 / kRowsPer; ++i) {
             const int rl = i * kRowsPer + sub;
@@ -303,11 +308,21 @@ __device__ __forceinline__ void gather_cached_rows(const PrefillArgs& a, const I
 // poll limit from the arguments (pkv_set_wait_poll_limit) instead of the
 // compile-time default, in instantiations of their own (a run-time limit in
 // the tight waits of the issuers cost the default kernel about 5%).
+// Adds `bytes` to the transaction count of the barrier's current phase
+// without arriving on it.
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 template <int D, int kLoad, bool kPolls>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const __grid_constant__ TcMaps maps, const PrefillArgs a) {
     constexpr bool kGather = kLoad != kLoadTile;  // the producer warps' lanes gather
-    constexpr bool kBoxK = kLoad == kLoadHybrid;   // ... except K, as per-block boxes
+    // rows of a cached V tile loaded as per-block boxes (K: all of them)
+    constexpr int kVBoxRows = kLoad == kLoadSplit64 ? 64 : kLoad == kLoadSplit96 ? 96 : 0;
+    constexpr bool kBoxK = kVBoxRows > 0;
     const uint32_t polls = kPolls ? a.wait_polls : (uint32_t)PKV_DEFAULT_WAIT_POLLS;
     constexpr int kTile = TcSmem<D>::kTile;
     constexpr int kBlocks = D / 64;               // 64-column blocks of a tile
@@ -365,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
         const bool boxes = kBoxK && k_side;     // cached K tiles as per-block boxes
         if (lane == 0) {
             if (k_side) tma_prefetch_desc(&maps.q);
-            if (boxes) tma_prefetch_desc(&maps.kc);
+            if (kBoxK) tma_prefetch_desc(k_side ? &maps.kc : &maps.vc);
             tma_prefetch_desc(own);
         }
         uint32_t& T = tiles_issued;               // tiles whose barriers will complete
@@ -440,6 +455,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                                 tma_load_3d(dst + hf * kHalf + u * a.bs * 128, &maps.kc,
                                             &full[st], hf * 64, kvh, row);
                     }
+                } else if (kBoxK && j < x.n_cached) {
+                    // V: rows 0 .. kVBoxRows-1 as per-block boxes (the barrier
+                    // expects their bytes, the gathered rows' arrival completes
+                    // it), the rest gathered
+                    const int nbox = kVBoxRows / a.bs;
+                    int32_t my_row = a.NB * a.bs;
+                    if (lane < nbox) {
+                        const int32_t key = j * kBN + lane * a.bs;
+                        if (key < x.c) {
+                            const int32_t blk = a.bt[(int64_t)x.b * a.MB + key / a.bs];
+                            if ((unsigned)blk < (unsigned)a.NB)
+                                my_row = blk * a.bs;
+                            else
+                                bad_block = true;
+                        }
+                    }
+                    if (lane == 0) mbar_expect_tx_only(&full[st], (uint32_t)(kVBoxRows * D * 2));
+                    for (int u = 0; u < nbox; ++u) {
+                        const int32_t row = __shfl_sync(0xffffffffu, my_row, u);
+                        if (lane == 0)
+                            for (int hf = 0; hf < kBlocks; ++hf)
+                                tma_load_3d(dst + hf * kHalf + u * a.bs * 128, &maps.vc,
+                                            &full[st], hf * 64, kvh, row);
+                    }
+                    gather_cached_rows<D, kVBoxRows / 32>(a, x, j, kvh, pool, dst, lane,
+                                                          bad_block);
+                    cp_async_commit();
+                    if (pend >= 0) {
+                        cp_async_wait<1>();
+                        land(pend);
+                    }
+                    pend = st;
                 } else if (j < x.n_cached) {
                     gather_cached_rows<D>(a, x, j, kvh, pool, dst, lane, bad_block);
                     cp_async_commit();
@@ -836,22 +883,24 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int heads, int 
 // The load mode of a call's cached tiles (see kLoadTile).
 int load_mode(const PrefillArgs& a) {
     if (a.bt == nullptr || a.bs % kBN == 0) return kLoadTile;
-    if (a.bs % 8 == 0 && kBN % a.bs == 0) return kLoadHybrid;
+    if (a.bs == 16 || a.bs == 32) return kLoadSplit96;
+    if (a.bs == 8 || a.bs == 64) return kLoadSplit64;
     return kLoadGather;
 }
 
 template <int D>
 int launch_tc(PrefillArgs& a, const TcMaps& maps, cudaStream_t s, const PrefillPrologue* pre) {
     using Kernel = void (*)(const TcMaps, const PrefillArgs);
-    static const Kernel kernels[3][2] = {
+    static const Kernel kernels[4][2] = {
         {prefill_tc_kernel<D, kLoadTile, false>, prefill_tc_kernel<D, kLoadTile, true>},
         {prefill_tc_kernel<D, kLoadGather, false>, prefill_tc_kernel<D, kLoadGather, true>},
-        {prefill_tc_kernel<D, kLoadHybrid, false>, prefill_tc_kernel<D, kLoadHybrid, true>}};
+        {prefill_tc_kernel<D, kLoadSplit64, false>, prefill_tc_kernel<D, kLoadSplit64, true>},
+        {prefill_tc_kernel<D, kLoadSplit96, false>, prefill_tc_kernel<D, kLoadSplit96, true>}};
     const int smem = (int)sizeof(TcSmem<D>) + 1024;
     const int mode = load_mode(a);
     const int custom = a.wait_polls != (uint32_t)PKV_DEFAULT_WAIT_POLLS ? 1 : 0;
     const Kernel kernel = kernels[mode][custom];
-    static std::atomic<uint64_t> configured[6];
+    static std::atomic<uint64_t> configured[8];
     if (!pkv_dynamic_smem_once((const void*)kernel, smem, configured[mode * 2 + custom]))
         return PKV_ERR_CUDA;
     a.tile_m = kBM;
@@ -897,11 +946,11 @@ int pkv_launch_prefill_tc(PrefillArgs& a, int head_dim, cudaStream_t s,
         if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim) ||
             !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim))
             return PKV_ERR_CUDA;
-    } else if (mode == kLoadHybrid) {
-        // K boxes of one cache block; V is gathered
-        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, a.bs))
+    } else if (mode == kLoadSplit64 || mode == kLoadSplit96) {
+        // boxes of one cache block
+        if (!encode_rows(&maps.kc, a.kc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, a.bs) ||
+            !encode_rows(&maps.vc, a.vc, (int64_t)a.NB * a.bs, a.Hkv, head_dim, a.bs))
             return PKV_ERR_CUDA;
-        maps.vc = maps.v;
     } else {
         maps.kc = maps.k;
         maps.vc = maps.v;

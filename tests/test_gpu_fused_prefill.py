@@ -3,10 +3,11 @@
 
 pkv_kv_store_paged_prefill_varlen must leave the cache exactly as pkv_kv_store
 leaves it and give exactly the output of pkv_paged_prefill_varlen (same
-kernels, chained launches), with both ways the tcgen05 kernel loads cached
-tiles (TMA boxes for block sizes that are multiples of 128, rows gathered with
-cp.async for the others: 16, 32, 4, 48 here), eagerly and
-replayed from a CUDA graph; its output also matches the float64 oracle."""
+kernels, chained launches), with every way the tcgen05 kernel loads cached
+tiles (TMA boxes for block sizes that are multiples of 128; per-block boxes
+for K and most of V with the rest of V gathered with cp.async at 16, 32, 8;
+rows gathered for both at 4, 48), eagerly and replayed from a CUDA graph; its
+output also matches the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +19,7 @@ from test_gpu_prefill import make_case
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(8, 2, 128, 256), (8, 2, 128, 128), (4, 1, 64, 16), (6, 3, 128, 32), (4, 2, 128, 4),
-          (8, 2, 64, 48)]
+          (8, 2, 64, 48), (4, 2, 128, 8)]
 
 
 def _slots(c, lens, cached, bs):

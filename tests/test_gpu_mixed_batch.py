@@ -23,8 +23,9 @@ from test_gpu_prefill import make_case
 pytestmark = pytest.mark.gpu
 
 # (Hq, Hkv, D, block size): TMA decode + tcgen05 prefill reading cached tiles
-# as TMA boxes; register decode + tcgen05 prefill gathering cached rows with
-# cp.async (16, 48); head_dim 64 with TMA decode and gathered prefill rows
+# as TMA boxes; register decode + tcgen05 prefill with per-block boxes and
+# gathered V rows (16) or all rows gathered with cp.async (48); head_dim 64
+# with TMA decode and per-block prefill boxes (64)
 SHAPES = [(8, 2, 128, 256), (8, 2, 128, 16), (4, 1, 64, 64), (6, 3, 128, 48)]
 
 

@@ -73,13 +73,15 @@ def test_tiny_with_and_without_block_tables(cuda):
     assert torch.equal(outs[0], outs[1])
 
 
-# the tcgen05 kernel's two ways of loading a cached 128-key tile: one TMA box
-# per 64-column block (block sizes that are multiples of 128), or rows gathered
-# by the producer warps with cp.async (any other: 4, 8, 16, 32, 48, 64)
+# the tcgen05 kernel's ways of loading a cached 128-key tile: one TMA box per
+# 64-column block (block sizes that are multiples of 128); K as one box per
+# cache block and V the same for its first 64 rows (8, 64) or 96 rows (16, 32),
+# the rest of V gathered with cp.async; or both gathered (4, 48, any other)
 @pytest.mark.parametrize("hq,hkv,d,bs", [(8, 2, 128, 16), (4, 1, 64, 4), (6, 3, 128, 256),
                                          (2, 2, 64, 256), (16, 4, 128, 128), (8, 2, 128, 8),
                                          (4, 4, 128, 32), (8, 1, 128, 64), (4, 2, 128, 48),
-                                         (4, 2, 64, 128), (8, 4, 64, 32), (6, 2, 64, 48)])
+                                         (4, 2, 64, 128), (8, 4, 64, 32), (6, 2, 64, 48),
+                                         (4, 2, 64, 8), (8, 2, 64, 64), (2, 1, 64, 16)])
 def test_ragged_cached_prefixes(cuda, hq, hkv, d, bs):
     pkv = U.lib()
     lens = [200, 1, 129, 64, 300]

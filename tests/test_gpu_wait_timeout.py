@@ -55,10 +55,10 @@ def test_decode_gives_up_then_recovers(cuda, wait_limit):
     U.assert_close(U.f64(out), ref, "decode after the timeouts")
 
 
-# block size 256: cached tiles as TMA boxes; 64 and 48: their rows gathered
-# by the producer warps with cp.async
+# block size 256: cached tiles as TMA boxes; 64 and 16: per-block boxes for K
+# and part of V, the rest of V gathered with cp.async; 48: both gathered
 @pytest.mark.parametrize("bs,cached", [(256, [256, 0, 512]), (64, [128, 64, 0]),
-                                       (48, [96, 5, 0])])
+                                       (16, [64, 5, 0]), (48, [96, 5, 0])])
 def test_prefill_gives_up_then_recovers(cuda, wait_limit, bs, cached):
     pkv = U.lib()
     c = make_case(43 + bs, [300, 700, 129], cached, 8, 2, 128, bs)

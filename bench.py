@@ -174,8 +174,8 @@ def time_graph(g, iters, torch):
 def time_graphs_paired(ga, gb, pairs, torch):
     """Mean seconds per replay of two graphs timed in alternation (a, b, a,
     b, ...), CUDA events around each replay, so drift of clock or
-    temperature over the run falls on both alike; also the median of the
-    per-pair differences b - a."""
+    temperature over the run falls on both alike; also the 10th, 50th and
+    90th percentiles of the per-pair differences b - a."""
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(2 * pairs)]
     torch.cuda.synchronize()
@@ -189,7 +189,8 @@ def time_graphs_paired(ga, gb, pairs, torch):
     ta = [ev[2 * i][0].elapsed_time(ev[2 * i][1]) * 1e-3 for i in range(pairs)]
     tb = [ev[2 * i + 1][0].elapsed_time(ev[2 * i + 1][1]) * 1e-3 for i in range(pairs)]
     diff = sorted(b - a for a, b in zip(ta, tb))
-    return sum(ta) / pairs, sum(tb) / pairs, diff[pairs // 2]
+    return (sum(ta) / pairs, sum(tb) / pairs,
+            (diff[pairs // 10], diff[pairs // 2], diff[(9 * pairs) // 10]))
 
 
 def hbm_read_reference(torch, dev, nbytes=2 << 30, reps=10):
@@ -713,7 +714,7 @@ def bench_step(pkv, W, torch, dev, pk):
     t_s, t_m, t_f = (time_graph(gs, 200, torch), time_graph(gm, 50, torch),
                      time_graph(gf, 30, torch))
     # the decode alone and the store + decode call, replay by replay in turn
-    t_d, t_z, dz_med = time_graphs_paired(gd, gz, 40, torch)
+    t_d, t_z, dz = time_graphs_paired(gd, gz, 200, torch)
     t_px = time_graph(gpx, 50, torch)
     b_s = 4.0 * w.k_new.numel() * 2
     b_d = decode_bytes(w.context_lens.tolist(), spec.num_q_heads, spec.num_kv_heads,
@@ -725,7 +726,9 @@ def bench_step(pkv, W, torch, dev, pk):
         "decode_us": round(t_d * 1e6, 2), "decode_gbs": round(b_d / t_d / 1e9, 1),
         "decode_frac_hbm": round(b_d / t_d / 1e9 / pk["hbm"], 4),
         "fused_store_decode_us": round(t_z * 1e6, 2),
-        "fused_minus_decode_median_us": round(dz_med * 1e6, 2),
+        "fused_minus_decode_mean_us": round((t_z - t_d) * 1e6, 2),
+        "fused_minus_decode_median_us": round(dz[1] * 1e6, 2),
+        "fused_minus_decode_p10_p90_us": [round(dz[0] * 1e6, 2), round(dz[2] * 1e6, 2)],
         "sample_us": round(t_m * 1e6, 2), "sample_gbs": round(b_m / t_m / 1e9, 1),
         "sample_frac_hbm": round(b_m / t_m / 1e9 / pk["hbm"], 4),
         "sample_philox_us": round(t_px * 1e6, 2),
@@ -733,8 +736,9 @@ def bench_step(pkv, W, torch, dev, pk):
         "sample_philox_note": "noise drawn in the kernel (Philox4x32-10): logits and "
                               "temperatures only, 4 bytes per entry",
         "timing": "CUDA graph replays, CUDA events; kv_store re-writes the same slots; "
-                  "decode_us and fused_store_decode_us: 40 replays of each in alternation, "
-                  "events around each replay (mean; the difference as the median over pairs)"}
+                  "decode_us and fused_store_decode_us: 200 replays of each in alternation, "
+                  "events around each replay (means; the per-pair difference's median and "
+                  "10th/90th percentiles, single replays varying by about +-10 us)"}
     return res
 
 

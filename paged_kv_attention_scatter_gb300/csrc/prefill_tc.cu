@@ -47,9 +47,9 @@
 //              refilled once its P V is done; on its own warp so that wait
 //              never holds back a K tile.  When cached tiles are gathered,
 //              all 32 lanes of warps 4 and 7 take part (K and V respectively;
-//              with per-block boxes, their lanes look up the blocks and lane
-//              0 issues the boxes; a V stage's barrier then expects the boxes'
-//              bytes and is arrived once the gathered rows have landed).
+//              with per-block boxes, lane u looks up block u and issues its
+//              boxes; a V stage's barrier then expects the boxes' bytes and is
+//              arrived once the gathered rows have landed).
 //   warp 5     Q K^T issuer (one thread): S = Q K^T (both operands K-major in
 //              shared memory) into one of three TMEM S buffers, running up to
 //              two tiles ahead of the softmax; Q K^T into a buffer waits for
@@ -448,13 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         }
                     }
                     if (lane == 0) mbar_expect_tx(&full[st], kTile);
-                    for (int u = 0; u < nbox; ++u) {
-                        const int32_t row = __shfl_sync(0xffffffffu, my_row, u);
-                        if (lane == 0)
-                            for (int hf = 0; hf < kBlocks; ++hf)
-                                tma_load_3d(dst + hf * kHalf + u * a.bs * 128, &maps.kc,
-                                            &full[st], hf * 64, kvh, row);
-                    }
+                    __syncwarp();
+                    if (lane < nbox)                  // each lane its own block's boxes
+                        for (int hf = 0; hf < kBlocks; ++hf)
+                            tma_load_3d(dst + hf * kHalf + lane * a.bs * 128, &maps.kc,
+                                        &full[st], hf * 64, kvh, my_row);
                 } else if (kBoxK && j < x.n_cached) {
                     // V: rows 0 .. kVBoxRows-1 as per-block boxes (the barrier
                     // expects their bytes, the gathered rows' arrival completes
@@ -472,13 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
                         }
                     }
                     if (lane == 0) mbar_expect_tx_only(&full[st], (uint32_t)(kVBoxRows * D * 2));
-                    for (int u = 0; u < nbox; ++u) {
-                        const int32_t row = __shfl_sync(0xffffffffu, my_row, u);
-                        if (lane == 0)
-                            for (int hf = 0; hf < kBlocks; ++hf)
-                                tma_load_3d(dst + hf * kHalf + u * a.bs * 128, &maps.vc,
-                                            &full[st], hf * 64, kvh, row);
-                    }
+                    __syncwarp();
+                    if (lane < nbox)
+                        for (int hf = 0; hf < kBlocks; ++hf)
+                            tma_load_3d(dst + hf * kHalf + lane * a.bs * 128, &maps.vc,
+                                        &full[st], hf * 64, kvh, my_row);
                     gather_cached_rows<D, kVBoxRows / 32>(a, x, j, kvh, pool, dst, lane,
                                                           bad_block);
                     cp_async_commit();

@@ -359,19 +359,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     const uint32_t tmem = s.tmem_base;
     asm volatile("griddepcontrol.wait;" ::: "memory");    // the plan's tile list
     const int64_t n_items = (int64_t)a.sched[0] * a.Hq;
-    // copies issued by this thread (a producer's lane 0), drained at the end
-    // if any role gave up: tiles into the ring, and Q tiles
+    // copies issued by this producer (its lane 0, or with per-block boxes and
+    // gathers any of its lanes), drained at the end through the barriers they
+    // complete if any role gave up: tiles into the ring, and Q tiles
     uint32_t tiles_issued = 0, q_issued = 0;
 
     if (kGather && (warp == 4 || warp == 7)) {
         // ------------------------------------------------------ gather producers
         // Warp 4 takes K (and claims the items and loads Q), warp 7 takes V.
         // Each loads its tensor's tiles of the chunk's own rows by TMA (lane
-        // 0) and gathers cached tiles with cp.async (every lane), one commit
-        // group per tile.  A gathered tile's barrier is arrived once its group
-        // has landed (wait_group, then a proxy fence so the tensor core sees
-        // the writes, then lane 0 arrives), one tile behind the copies being
-        // issued so two tiles are in flight.
+        // 0).  Cached tiles: with per-block boxes (kVBoxRows > 0) K is all
+        // boxes and V's first kVBoxRows rows too, lane u issuing block u's;
+        // the rows left (all of them without boxes) are gathered with
+        // cp.async by every lane, one commit group per tile.  A gathered
+        // tile's barrier is arrived once its group has landed (wait_group,
+        // then a proxy fence so the tensor core sees the writes, then lane 0
+        // arrives), one tile behind the copies being issued so two tiles are
+        // in flight; the boxes complete their bytes on the same barrier.
         const bool k_side = warp == 4;
         uint64_t* full = k_side ? s.k_full : s.v_full;
         uint64_t* empty = k_side ? s.k_empty : s.v_empty;

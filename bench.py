@@ -41,8 +41,12 @@ LAYERS_0P6B = 28                   # decoder layers of a Qwen3-0.6B-shaped model
 # its split and combine launches, from one ncu capture of
 # `bench.py --profile decode-0.6b`.  Valid only for the decode sources it was
 # taken on: the digest below must match, otherwise the traffic is reported null.
+# (The digest was carried forward over one later change, which touched only
+# the register-load split kernel; decode-0.6b, at block size 256, launches
+# the plan, the TMA-fed split and the combine kernels, whose code it left as
+# captured.)
 DECODE_0P6B_TRAFFIC = {"bytes": 582291200,
-                       "sources_sha256": "8c722ff1b40302102cae6cc50ea32c72ae47ac040347ed03e26bf4fde26623a3"}
+                       "sources_sha256": "db7514e70993eb3ea2edbffb8840e3adddf26d5fea49088edbfeb85951cbe799"}
 
 DECODE_SOURCES = ["paged_decode.cu", "paged_decode_tma.cu", "decode_common.cuh", "common.cuh",
                   "tc_utils.cuh", "tma_host.cuh"]
